@@ -1,0 +1,464 @@
+#!/usr/bin/env python3
+"""Bench: MXFP4 weight-streaming decode/verify step on GB300.
+
+One step = one weight-streaming call over one batch of decode tokens
+(default workload: T=4 verify step, K=N=7168 dense projection). Prints one
+JSON line (rank 0). Metric: effective HBM GB/s, where bytes = 0.53125*N*K
+(packed weights + scales actually read) + 2*T*K (x) + 2*T*N (y).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--sweep]
+
+Timing: the timed steps are a CUDA-graph replay of back-to-back calls that
+cycle through enough independent weight copies to exceed 2x L2, so every
+call streams its weights from HBM; CUDA events on the launching stream
+bracket the region (device time), and per-launch events give the kernel's
+average duration for the roofline. Clocks are sampled with nvidia-smi while
+the workload runs.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "effective HBM GB/s (% of GB300 peak) and us/call, MXFP4 GEMM at T=1-32"
+FALLBACK_HBM_GBS = 6800.0  # fallback peak when no measured peak file is present
+KERNEL_SOURCES = ["mxfp4_weight_streaming_gb300/csrc/linear.cu", "mxfp4_weight_streaming_gb300/csrc/device_common.cuh"]
+
+WORKLOADS = {
+    "linear_t1_k1024_n1024": dict(t=1, k=1024, n=1024, seed=0, x64=False),
+    "verify_t4_k7168_n7168": dict(t=4, k=7168, n=7168, seed=1, x64=False),
+    "lmhead_t4_k7168_n129280": dict(t=4, k=7168, n=129280, seed=2, x64=True),
+    "ffn_up_t1_k7168_n18432": dict(t=1, k=7168, n=18432, seed=3, x64=False),
+    "ffn_up_t2_k7168_n18432": dict(t=2, k=7168, n=18432, seed=3, x64=False),
+    "ffn_up_t4_k7168_n18432": dict(t=4, k=7168, n=18432, seed=3, x64=False),
+    "ffn_up_t8_k7168_n18432": dict(t=8, k=7168, n=18432, seed=3, x64=False),
+    "ffn_up_t16_k7168_n18432": dict(t=16, k=7168, n=18432, seed=3, x64=False),
+    "ffn_up_t32_k7168_n18432": dict(t=32, k=7168, n=18432, seed=3, x64=False),
+}
+DEFAULT_WORKLOAD = "verify_t4_k7168_n7168"
+
+
+def algorithmic_bytes(t: int, k: int, n: int) -> int:
+    return n * k // 2 + n * k // 32 + 2 * t * k + 2 * t * n
+
+
+def kernel_digest() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def hbm_peak():
+    """(GB/s, source) from the measured-peaks file, else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            for key in ("hbm_gbs", "hbm_GBps", "hbm_gb_s", "copy_gbs"):
+                if key in d:
+                    return float(d[key]), "measured"
+            for v in d.values():
+                if isinstance(v, dict):
+                    for key in ("hbm_gbs", "hbm_GBps"):
+                        if key in v:
+                            return float(v[key]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic(workload: str):
+    """dram bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        d = json.load(open(path))
+        ent = d.get(workload)
+        if ent and ent.get("kernel_digest") == kernel_digest():
+            return int(ent["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        rows = [p for (ts, p) in self.samples if t0 <= ts <= t1] or [p for (_, p) in self.samples]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(name)
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_median": statistics.median(power) if power else None}
+
+
+# ---------------------------------------------------------------- our arm
+def setup_dense(wl: dict, device):
+    import torch
+
+    import mxfp4_weight_streaming_gb300 as mx
+    import synth
+
+    t, k, n = wl["t"], wl["k"], wl["n"]
+    w = synth.weights(wl["seed"], n, k, device=device, x64_blocks=wl["x64"])
+    wq, ws = mx.quantize(w)
+    del w
+    x = synth.tokens(wl["seed"], t, k, device=device)
+    y = torch.empty((t, n), dtype=torch.bfloat16, device=device)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    wbytes = wq.numel() + ws.numel()
+    copies = max(1, math.ceil(2 * l2 / wbytes) + 1) if wbytes < 2 * l2 else 1
+    wqs = [wq] + [wq.clone() for _ in range(copies - 1)]
+    wss = [ws] + [ws.clone() for _ in range(copies - 1)]
+    torch.cuda.synchronize()
+    return dict(x=x, y=y, wqs=wqs, wss=wss, copies=copies, t=t, k=k, n=n, l2=l2)
+
+
+def run_ours(args, wl_name: str, rank: int, world: int, device, with_cpu_baseline: bool):
+    import torch
+
+    import mxfp4_weight_streaming_gb300 as mx
+
+    wl = WORKLOADS[wl_name]
+    st = setup_dense(wl, device)
+    t, k, n = st["t"], st["k"], st["n"]
+    stream = torch.cuda.Stream(device)
+    sp = stream.cuda_stream
+    lib = mx.load()
+    xp, yp = st["x"].data_ptr(), st["y"].data_ptr()
+    wq_ptrs = [a.data_ptr() for a in st["wqs"]]
+    ws_ptrs = [a.data_ptr() for a in st["wss"]]
+
+    def call(i):
+        rc = lib.mxfp4_linear(xp, t, k, wq_ptrs[i % st["copies"]], ws_ptrs[i % st["copies"]], n, yp, sp)
+        if rc != 0:
+            raise RuntimeError(mx.strerror(rc))
+
+    # Graph of G back-to-back calls with an event after each launch.
+    G = max(st["copies"], min(args.steps, 256 // st["copies"] * st["copies"] or st["copies"]))
+    G = min(G, max(1, args.steps))
+    try:
+        events = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(G + 1)]
+    except TypeError:  # older torch: no event-record nodes inside graphs
+        events = None
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            call(i)  # first calls set per-device state before capture
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        if events:
+            events[0].record(stream)
+        for i in range(G):
+            call(i)
+            if events:
+                events[i + 1].record(stream)
+    rem = args.steps % G
+    graph_rem = None
+    if rem:
+        graph_rem = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_rem, stream=stream):
+            for i in range(rem):
+                call(i)
+    n_full = args.steps // G
+
+    clocks = ClockSampler(torch.cuda.current_device() if os.environ.get("CUDA_VISIBLE_DEVICES") is None
+                          else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[0]))
+    clocks.start()
+    # Soak: keep the GPU on this workload for ~1 s so clock samples mean something.
+    soak_end = time.time() + 1.0
+    with torch.cuda.stream(stream):
+        while time.time() < soak_end:
+            graph.replay()
+            stream.synchronize()
+        w_left = args.warmup
+        while w_left > 0:
+            if w_left >= G:
+                graph.replay()
+                w_left -= G
+            else:
+                for i in range(w_left):
+                    call(i)
+                w_left = 0
+    stream.synchronize()
+
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    per_launch = []
+    wall0 = time.time()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(n_full):
+            graph.replay()
+            # per-launch durations of this replay (events inside the graph)
+        if graph_rem is not None:
+            graph_rem.replay()
+        end.record(stream)
+    end.synchronize()
+    wall1 = time.time()
+    torch.cuda.synchronize()
+    if n_full and events:
+        per_launch = [events[i].elapsed_time(events[i + 1]) for i in range(G)]
+    elapsed_ms = start.elapsed_time(end)
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], device=device, dtype=torch.float64)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        torch.distributed.barrier()
+        elapsed_ms = float(tt.item())
+    clocks.stop()
+
+    # End to end through the public API: pinned host x in, host y out, every step.
+    x_host = st["x"].cpu().pin_memory()
+    y_host = torch.empty((t, n), dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(1, min(args.steps, 2000))
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            st["x"].copy_(x_host, non_blocking=True)
+            mx.linear(st["x"], st["wqs"][i % st["copies"]], st["wss"][i % st["copies"]], out=st["y"], stream=stream)
+            y_host.copy_(st["y"], non_blocking=True)
+        stream.synchronize()
+        e0 = time.perf_counter()
+        for i in range(e2e_steps):
+            st["x"].copy_(x_host, non_blocking=True)
+            mx.linear(st["x"], st["wqs"][i % st["copies"]], st["wss"][i % st["copies"]], out=st["y"], stream=stream)
+            y_host.copy_(st["y"], non_blocking=True)
+            stream.synchronize()
+        e1 = time.perf_counter()
+
+    bytes_call = algorithmic_bytes(t, k, n)
+    us_call = elapsed_ms * 1e3 / args.steps
+    value = bytes_call * args.steps * world / (elapsed_ms * 1e-3) / 1e9
+    peak, peak_src = hbm_peak()
+    avg_launch_ms = statistics.mean(per_launch) if per_launch else elapsed_ms / args.steps
+    achieved = bytes_call / (avg_launch_ms * 1e-3) / 1e9
+    e2e_us = (e1 - e0) * 1e6 / e2e_steps
+    res = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / args.steps,
+        "us_per_call": round(us_call, 4),
+        "pct_of_peak": round(100.0 * value / world / peak, 2),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "mxfp4xbf16->f32",
+        "data": "synthetic (seeded counter-based N(0,0.02) weights, N(0,1) bf16 tokens)",
+        "config": {"workload": wl_name, "T": t, "K": k, "N": n, "bytes_per_call": bytes_call,
+                   "weight_copies": st["copies"], "l2_bytes": st["l2"],
+                   "l2_policy": "rotating weight copies (> 2x L2) so every call streams from HBM",
+                   "timing": f"CUDA graph of {G} calls, device events", "parallelism": f"replicas x{world}"},
+        "e2e": {"value": round(bytes_call / (e2e_us * 1e-6) / 1e9, 2), "unit": "GB/s", "us_per_call": round(e2e_us, 3),
+                "h2d_bytes_per_step": 2 * t * k, "d2h_bytes_per_step": 2 * t * n},
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(wl_name),
+                     "peak_source": f"{peak_src} (HBM copy bandwidth)",
+                     "kernel": "mxfp4::linear_kernel", "avg_launch_us": round(avg_launch_ms * 1e3, 4),
+                     "algorithmic_bytes_per_launch": bytes_call},
+        "clocks": clocks.summary(wall0 - 1.5, wall1 + 0.1),
+    }
+    if with_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(wl_name)
+    return res
+
+
+# ------------------------------------------------------- CPU oracle timing
+def cpu_baseline(wl_name: str, budget_s: float = 12.0):
+    """The oracle, as it stands, on this host's cores, on a bounded sample:
+    the workload's full call if it fits the budget, else a row subset scaled
+    to the same metric (GB/s of the same algorithmic bytes)."""
+    import numpy as np
+
+    import oracle
+    import synth
+
+    wl = WORKLOADS[wl_name]
+    t, k, n = wl["t"], wl["k"], wl["n"]
+    rows = n
+    # weights for the sampled rows only (CPU generation)
+    probe = min(n, 512)
+    w = synth.weights(wl["seed"], probe, k, x64_blocks=wl["x64"]).numpy()
+    wq, ws = oracle.quantize(w)
+    x = synth.tokens(wl["seed"], t, k)
+    t0 = time.perf_counter()
+    oracle.linear(x, wq, ws)
+    dt = time.perf_counter() - t0
+    per_row = dt / probe
+    rows = int(min(n, max(probe, budget_s / max(per_row, 1e-9))))
+    if rows > probe:
+        w = synth.weights(wl["seed"], rows, k, x64_blocks=wl["x64"]).numpy()
+        wq, ws = oracle.quantize(w)
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.linear(x, wq, ws)
+        reps += 1
+        if time.perf_counter() - t0 > budget_s / 2 or reps >= 50:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    frac = rows / n
+    bytes_sample = algorithmic_bytes(t, k, n) * frac
+    gbs = bytes_sample / dt / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{rows} of {n} output rows, all {t} tokens, {reps} repetition(s); "
+                      f"{dt * 1e3:.1f} ms per sample ({dt / frac * 1e3:.1f} ms per full call)"}
+
+
+def run_reference(args, wl_name: str):
+    """The reference arm: the CPU oracle timed on this host (no reference
+    implementation exists to install); bounded so the run ends in minutes."""
+    t_start = time.time()
+    wl = WORKLOADS[wl_name]
+    steps_budget = max(5.0, 60.0 / max(1, args.steps + args.warmup))
+    cb = cpu_baseline(wl_name, budget_s=min(12.0, steps_budget))
+    value = cb["value"]
+    t, k, n = wl["t"], wl["k"], wl["n"]
+    bytes_call = algorithmic_bytes(t, k, n)
+    ms = bytes_call / (value * 1e9) * 1e3 if value > 0 else None
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded)",
+        "config": {"workload": wl_name, "T": t, "K": k, "N": n, "bytes_per_call": bytes_call},
+        "cpu_baseline": cb,
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": round(time.time() - t_start, 2),
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--sweep", action="store_true", help="also time every other dense workload (extra key)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, args.workload)), flush=True)
+        return
+
+    import torch
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=device)
+    import mxfp4_weight_streaming_gb300 as mx
+    from mxfp4_weight_streaming_gb300 import build as b
+    if rank == 0:
+        b.build()
+    if world > 1:
+        torch.distributed.barrier()
+    mx.load()
+    res = run_ours(args, args.workload, rank, world, device, with_cpu_baseline=(rank == 0 and world == 1
+                                                                                 and not args.no_cpu_baseline))
+    if args.sweep and rank == 0:
+        sweep = {}
+        sub = argparse.Namespace(**vars(args))
+        sub.steps = min(args.steps, 4000)
+        sub.warmup = 50
+        for name in WORKLOADS:
+            if name == args.workload:
+                continue
+            try:
+                r = run_ours(sub, name, 0, 1, device, with_cpu_baseline=False)
+                sweep[name] = {"us_per_call": r["us_per_call"], "GBps": r["value"], "pct_of_peak": r["pct_of_peak"],
+                               "roofline_frac": r["roofline"]["frac"], "avg_launch_us": r["roofline"]["avg_launch_us"]}
+            except Exception as ex:  # report, do not hide
+                sweep[name] = {"error": str(ex)[:200]}
+            torch.cuda.empty_cache()
+        res["sweep"] = sweep
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,146 @@
+/*
+ * mxfp4.h -- C ABI of the GB300 (sm_103a) MXFP4 weight-streaming library.
+ *
+ * The decode / speculative-verify step reads every weight it needs from HBM
+ * once and applies it to the handful of tokens in the step ("Zyphra
+ * Inference Wave 2", section "Speculative decoding"; AMD "megakernel-intro",
+ * section "3. Low-Precision Data Types"). Weights are MXFP4: blocks of 32
+ * E2M1 values (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 with a sign bit) that
+ * share one E8M0 power-of-two scale, 4.25 bits per value ("Zyphra Inference
+ * Wave 2", section "Quantization"). Activations are bf16 and outputs bf16
+ * with fp32 accumulation (the a16w4 kernel of "Zyphra Inference Wave 2",
+ * section "Kernel Results").
+ *
+ * Packed layout (shared by every entry point):
+ *   wq  uint8 [rows, K/2]   byte j of a row holds the code of column 2j in
+ *                           its low nibble and of column 2j+1 in its high
+ *                           nibble; code bit 3 is the sign.
+ *   ws  uint8 [rows, K/32]  E8M0 byte s of each 32-column block: 2^(s-127).
+ *
+ * Conventions for every call:
+ *   - All pointers are device memory owned by the caller. The library
+ *     allocates nothing; the MoE scratch comes from the caller's workspace.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls
+ *     only enqueue work and return; results are ready when the stream is.
+ *   - Argument errors are returned before anything is launched. A failed
+ *     launch returns MXFP4_ERR_CUDA.
+ *   - Kernels never spin unboundedly: every wait gives up after about two
+ *     seconds, sets a per-device status word and lets the kernel exit.
+ *     mxfp4_last_device_status() reports (and clears) that word.
+ *   - Identical inputs give bit-identical outputs (no floating-point
+ *     atomics); calls are stateless and thread-safe apart from the
+ *     caller's own buffers.
+ *   - There is no CPU path: without a GB300-class GPU every compute call
+ *     returns MXFP4_ERR_CUDA.
+ */
+#ifndef MXFP4_H
+#define MXFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MXFP4_OK = 0,
+    MXFP4_ERR_INVALID_ARG = 1, /* null pointer, negative or zero size     */
+    MXFP4_ERR_SHAPE = 2,       /* a size the kernels do not support       */
+    MXFP4_ERR_ALIGN = 3,       /* a pointer is not aligned as documented  */
+    MXFP4_ERR_WORKSPACE = 4,   /* workspace missing or too small          */
+    MXFP4_ERR_CUDA = 5,        /* CUDA runtime or launch failure          */
+    MXFP4_ERR_TIMEOUT = 6      /* a device-side bounded wait expired      */
+} mxfp4_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* mxfp4_strerror(int status);
+
+/*
+ * MXFP4 packer ("Zyphra Inference Wave 2", section "Quantization"; the OCP
+ * MX rule for the shared scale). For every 32-value block of a row:
+ * amax = max |w|, s = clamp(floor(log2 amax) - 2 + 127, 0, 254) (0 for an
+ * all-zero block), each value w * 2^(127-s) rounded to the nearest E2M1
+ * point with ties to even and saturation at 6, keeping its sign bit.
+ *   w   device float32 [n, k], row-major, 16-byte aligned, finite values
+ *   n   rows (>= 1);  k  columns (>= 32, k % 32 == 0)
+ *   wq  device uint8 [n, k/2], 16-byte aligned (output)
+ *   ws  device uint8 [n, k/32] (output)
+ * Bit-exact with the oracle. NaN/Inf inputs are not supported (their codes
+ * are unspecified).
+ */
+int mxfp4_quantize(const float* w, int64_t n, int64_t k, uint8_t* wq, uint8_t* ws, void* stream);
+
+/*
+ * Weight-streaming linear layer, dense and LM-head shapes ("Zyphra
+ * Inference Wave 2", section "Speculative decoding": one target token plus
+ * drafts, or one token per concurrent request, per step):
+ *   y[t][j] = bf16( sum_k x[t][k] * w[j][k] ),  w = dequantized (wq, ws)
+ *   x   device bf16 [t, k], row-major, 16-byte aligned
+ *   t   tokens, 1 <= t <= 32
+ *   k   reduction length, k % 32 == 0, k >= 32
+ *   wq  device uint8 [n, k/2], 16-byte aligned;  ws device uint8 [n, k/32],
+ *       16-byte aligned
+ *   n   output features (>= 1, < 2^31)
+ *   y   device bf16 [t, n], row-major, 2-byte aligned (output)
+ * Accumulation is fp32 (tensor-core fp32 accumulate); the summation order
+ * is the kernel's. Returns MXFP4_ERR_SHAPE when t * k is too large for the
+ * on-chip activation buffer of this device.
+ */
+int mxfp4_linear(const void* x, int64_t t, int64_t k, const uint8_t* wq, const uint8_t* ws, int64_t n,
+                 void* y, void* stream);
+
+/*
+ * Bytes of device workspace mxfp4_moe needs for t tokens, e experts,
+ * top_k experts per token, hidden size `hidden` and expert width `inter`.
+ */
+size_t mxfp4_moe_workspace_size(int64_t t, int64_t e, int top_k, int64_t hidden, int64_t inter);
+
+/*
+ * Grouped top-k mixture-of-experts layer with fused SwiGLU ("Zyphra
+ * Inference Wave 2", sections "Kernel Results" and "Quantization": at low
+ * concurrency a step reads only the routed experts' weights; each expert
+ * receives a few token rows). For each token t:
+ *   ids = the top_k largest router logits (descending, ties to the smaller
+ *         expert index), g = softmax over those top_k logits;
+ *   for each selected expert e: a = W1_e[0:inter] x_t (gate rows),
+ *         b = W1_e[inter:2*inter] x_t (up rows), h = SiLU(a) * b (fp32),
+ *         o = W2_e h;
+ *   y[t] = bf16( sum over the selected experts in selection order of g*o ).
+ * Only experts that some token selects have their weights read.
+ *   x              device bf16 [t, hidden], 16-byte aligned
+ *   t              tokens, 1 <= t <= 256
+ *   hidden, inter  multiples of 32 (hidden >= 32, inter >= 32)
+ *   router_logits  device float32 [t, e]
+ *   e              experts, top_k <= e <= 1024;  1 <= top_k <= 16
+ *   w1q, w1s       device uint8 [e, 2*inter, hidden/2], [e, 2*inter, hidden/32]
+ *                  (rows 0..inter-1 gate, inter..2*inter-1 up), 16-byte aligned
+ *   w2q, w2s       device uint8 [e, hidden, inter/2], [e, hidden, inter/32],
+ *                  16-byte aligned
+ *   y              device bf16 [t, hidden] (output)
+ *   topk_ids       optional device int32 [t, top_k] output (NULL = skip)
+ *   topk_w         optional device float32 [t, top_k] output (NULL = skip)
+ *   workspace      device scratch of at least mxfp4_moe_workspace_size()
+ *                  bytes, 256-byte aligned; its contents on entry do not
+ *                  matter and are overwritten.
+ * Routing indices are exact (bit-identical to the oracle); gate weights
+ * are fp32.
+ */
+int mxfp4_moe(const void* x, int64_t t, int64_t hidden, const float* router_logits, int64_t e, int top_k,
+              const uint8_t* w1q, const uint8_t* w1s, const uint8_t* w2q, const uint8_t* w2s, int64_t inter,
+              void* y, int32_t* topk_ids, float* topk_w, void* workspace, size_t workspace_bytes,
+              void* stream);
+
+/*
+ * Synchronizes `stream`, then returns MXFP4_OK, MXFP4_ERR_TIMEOUT if some
+ * kernel of this library on the current device gave up a bounded wait since
+ * the last call, or MXFP4_ERR_CUDA if the stream reports an error. Clears
+ * the device status word.
+ */
+int mxfp4_last_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP4_H */

@@ -1,0 +1,188 @@
+// C ABI of the MXFP4 weight-streaming library: argument checks, per-device
+// set-up (SM count, shared-memory limit, status word), TMA descriptors and
+// kernel launches. Every compute step runs in this library's kernels.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "device_common.cuh"
+#include "linear_launch.h"
+#include "moe_launch.h"
+#include "mxfp4.h"
+
+namespace {
+
+// Per-device status word: kernels OR in mxfp4::kStatusTimeout when a bounded
+// wait gives up. Read and cleared by mxfp4_last_device_status().
+__device__ unsigned g_status_word;
+
+struct DeviceInfo {
+    bool ready = false;
+    int num_sms = 0;
+    int max_smem = 0;
+    unsigned* status = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_mutex;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int device_info(DeviceInfo** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MXFP4_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo& d = g_devices[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return MXFP4_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return MXFP4_ERR_CUDA;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return MXFP4_ERR_CUDA;
+        d.status = static_cast<unsigned*>(p);
+        if (!g_encode) {
+            cudaDriverEntryPointQueryResult q;
+            void* fn = nullptr;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                    cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || !fn)
+                return MXFP4_ERR_CUDA;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        d.ready = true;
+    }
+    *out = &d;
+    return MXFP4_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Packed weights viewed as a 2D uint8 tensor [rows, k/2], boxes of
+// 16 rows x 128 bytes with the 128-byte swizzle.
+int encode_weight_map(CUtensorMap* map, const uint8_t* wq, int64_t rows, int64_t k) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(k / 2), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(k / 2)};
+    cuuint32_t box[2] = {128, 16};
+    cuuint32_t estride[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(wq), dims, strides, box,
+                          estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MXFP4_OK : MXFP4_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mxfp4_strerror(int status) {
+    switch (status) {
+        case MXFP4_OK: return "MXFP4_OK";
+        case MXFP4_ERR_INVALID_ARG: return "MXFP4_ERR_INVALID_ARG: null pointer or non-positive size";
+        case MXFP4_ERR_SHAPE: return "MXFP4_ERR_SHAPE: unsupported size";
+        case MXFP4_ERR_ALIGN: return "MXFP4_ERR_ALIGN: pointer not aligned as documented";
+        case MXFP4_ERR_WORKSPACE: return "MXFP4_ERR_WORKSPACE: workspace missing or too small";
+        case MXFP4_ERR_CUDA: return "MXFP4_ERR_CUDA: CUDA runtime or launch failure";
+        case MXFP4_ERR_TIMEOUT: return "MXFP4_ERR_TIMEOUT: a device-side bounded wait expired";
+        default: return "MXFP4: unknown status";
+    }
+}
+
+int mxfp4_quantize(const float* w, int64_t n, int64_t k, uint8_t* wq, uint8_t* ws, void* stream) {
+    if (!w || !wq || !ws || n <= 0 || k <= 0) return MXFP4_ERR_INVALID_ARG;
+    if (k % 32 != 0) return MXFP4_ERR_SHAPE;
+    if (!aligned(w, 16) || !aligned(wq, 16)) return MXFP4_ERR_ALIGN;
+    DeviceInfo* d = nullptr;
+    if (int rc = device_info(&d)) return rc;
+    cudaError_t e = mxfp4::launch_quantize(w, n, k, wq, ws, static_cast<cudaStream_t>(stream), d->num_sms);
+    return e == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
+}
+
+int mxfp4_linear(const void* x, int64_t t, int64_t k, const uint8_t* wq, const uint8_t* ws, int64_t n, void* y,
+                 void* stream) {
+    if (!x || !wq || !ws || !y || t <= 0 || k <= 0 || n <= 0) return MXFP4_ERR_INVALID_ARG;
+    if (k % 32 != 0 || t > 32 || n >= (int64_t(1) << 31) || k >= (int64_t(1) << 31)) return MXFP4_ERR_SHAPE;
+    if (!aligned(x, 16) || !aligned(wq, 16) || !aligned(ws, 16) || !aligned(y, 2)) return MXFP4_ERR_ALIGN;
+    DeviceInfo* d = nullptr;
+    if (int rc = device_info(&d)) return rc;
+    mxfp4::LinearParams p{};
+    if (!mxfp4::plan_linear(static_cast<int>(t), static_cast<int>(k), d->max_smem, &p.cl, &p.layout))
+        return MXFP4_ERR_SHAPE;
+    CUtensorMap map;
+    if (int rc = encode_weight_map(&map, wq, n, k)) return rc;
+    p.x = static_cast<const __nv_bfloat16*>(x);
+    p.ws = ws;
+    p.y = static_cast<__nv_bfloat16*>(y);
+    p.status = d->status;
+    p.T = static_cast<int>(t);
+    p.K = static_cast<int>(k);
+    p.N = static_cast<int>(n);
+    p.nblk = static_cast<int>(k / 32);
+    p.nkb = static_cast<int>((k + 255) / 256);
+    p.xcols = static_cast<int>(t);
+    p.n_rg = static_cast<int>((n + 15) / 16);
+    cudaError_t e = mxfp4::launch_linear(map, p, d->num_sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
+}
+
+size_t mxfp4_moe_workspace_size(int64_t t, int64_t e, int top_k, int64_t hidden, int64_t inter) {
+    if (t <= 0 || e <= 0 || top_k <= 0 || hidden <= 0 || inter <= 0) return 0;
+    return mxfp4::moe_workspace_bytes(t, e, top_k, hidden, inter);
+}
+
+int mxfp4_moe(const void* x, int64_t t, int64_t hidden, const float* router_logits, int64_t e, int top_k,
+              const uint8_t* w1q, const uint8_t* w1s, const uint8_t* w2q, const uint8_t* w2s, int64_t inter, void* y,
+              int32_t* topk_ids, float* topk_w, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!x || !router_logits || !w1q || !w1s || !w2q || !w2s || !y || t <= 0 || hidden <= 0 || e <= 0 ||
+        top_k <= 0 || inter <= 0)
+        return MXFP4_ERR_INVALID_ARG;
+    if (hidden % 32 != 0 || inter % 32 != 0 || t > 256 || e > 1024 || top_k > 16 || top_k > e)
+        return MXFP4_ERR_SHAPE;
+    if (e * 2 * inter >= (int64_t(1) << 31) || e * hidden >= (int64_t(1) << 31)) return MXFP4_ERR_SHAPE;
+    if (!aligned(x, 16) || !aligned(w1q, 16) || !aligned(w1s, 16) || !aligned(w2q, 16) || !aligned(w2s, 16) ||
+        !aligned(y, 2) || !aligned(router_logits, 4) || (topk_ids && !aligned(topk_ids, 4)) ||
+        (topk_w && !aligned(topk_w, 4)))
+        return MXFP4_ERR_ALIGN;
+    if (!workspace) return MXFP4_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return MXFP4_ERR_ALIGN;
+    if (workspace_bytes < mxfp4::moe_workspace_bytes(t, e, top_k, hidden, inter)) return MXFP4_ERR_WORKSPACE;
+    DeviceInfo* d = nullptr;
+    if (int rc = device_info(&d)) return rc;
+    mxfp4::MoeArgs a{};
+    a.x = static_cast<const __nv_bfloat16*>(x);
+    a.logits = router_logits;
+    a.w1q = w1q;
+    a.w1s = w1s;
+    a.w2q = w2q;
+    a.w2s = w2s;
+    a.y = static_cast<__nv_bfloat16*>(y);
+    a.topk_ids = topk_ids;
+    a.topk_w = topk_w;
+    a.workspace = workspace;
+    a.status = d->status;
+    a.T = static_cast<int>(t);
+    a.E = static_cast<int>(e);
+    a.top_k = top_k;
+    a.hidden = static_cast<int>(hidden);
+    a.inter = static_cast<int>(inter);
+    CUtensorMap map1, map2;
+    if (int rc = encode_weight_map(&map1, w1q, e * 2 * inter, hidden)) return rc;
+    if (int rc = encode_weight_map(&map2, w2q, e * hidden, inter)) return rc;
+    return mxfp4::launch_moe(map1, map2, a, d->num_sms, d->max_smem, static_cast<cudaStream_t>(stream));
+}
+
+int mxfp4_last_device_status(void* stream) {
+    DeviceInfo* d = nullptr;
+    if (int rc = device_info(&d)) return rc;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MXFP4_ERR_CUDA;
+    unsigned word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_status_word, sizeof word) != cudaSuccess) return MXFP4_ERR_CUDA;
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero) != cudaSuccess) return MXFP4_ERR_CUDA;
+    return (word & mxfp4::kStatusTimeout) ? MXFP4_ERR_TIMEOUT : MXFP4_OK;
+}
+
+}  // extern "C"

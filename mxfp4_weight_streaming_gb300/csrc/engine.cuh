@@ -1,0 +1,559 @@
+// The weight-streaming engine shared by the dense / LM-head linear kernel and
+// the two MoE expert kernels.
+//
+// A kernel streams a sequence of "units". A unit is one group of 16 weight
+// rows (or BOXES groups of 16 rows that share their activations, e.g. the
+// gate and up rows of one expert) over the whole reduction dimension K,
+// applied to a small set of activation columns (tokens). Consecutive units
+// with the same activation columns form a "chunk"; the activations of a
+// chunk are staged once into shared memory.
+//
+// One persistent CTA per SM, warp-specialised:
+//   producer warp : per unit, one bulk copy of the scale bytes of each row
+//                   group (16 rows x K/32 contiguous bytes) into a scale
+//                   ring; per 256-wide K step, BOXES 2D TMA loads of
+//                   16 rows x 128 bytes (SWIZZLE_128B) into one ring slot.
+//   consumer warps: K steps are dealt round-robin over the warps. Per
+//                   32-value block: ldmatrix -> hardware E2M1 -> f16 unpack
+//                   -> two m16n8k16 MMAs (fp32 accumulate) per 8-column
+//                   tile -> partial * 2^(s-127) * column factor into fp32
+//                   accumulators. Per unit, each warp writes its partials
+//                   to a double-buffered reduction area.
+//   reducer warp  : sums the warps' partials in a fixed order and runs the
+//                   problem's epilogue (deterministic, no atomics).
+// Every wait is bounded (see device_common.cuh); on a timeout the kernel
+// records it in the status word and winds down.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "device_common.cuh"
+#include "engine_layout.h"
+
+namespace mxfp4 {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kReducerWarp = kConsumerWarps;
+constexpr int kProducerWarp = kConsumerWarps + 1;
+constexpr int kThreads = (kConsumerWarps + 2) * 32;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kBoxBytes = 2048;  // 16 rows x 128 bytes = 16 rows x 256 K values
+constexpr int kRedStride = 20;   // floats per column row of the reduction area (16 + 4 pad)
+
+struct Bars {
+    uint32_t base;
+    uint32_t nslot, nss;
+    __device__ uint32_t full(uint32_t s) const { return base + 8 * s; }
+    __device__ uint32_t empty(uint32_t s) const { return base + 8 * (nslot + s); }
+    __device__ uint32_t sfull(uint32_t s) const { return base + 8 * (2 * nslot + s); }
+    __device__ uint32_t sempty(uint32_t s) const { return base + 8 * (2 * nslot + nss + s); }
+    __device__ uint32_t rfull(uint32_t b) const { return base + 8 * (2 * nslot + 2 * nss + b); }
+    __device__ uint32_t rempty(uint32_t b) const { return base + 8 * (2 * nslot + 2 * nss + 2 + b); }
+};
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, unsigned* status) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ------------------------------------------------------------------------
+// Activation staging helpers (used by the problems' stage()).
+//
+// A column is 32 values of one 32-block stored as f16 = v * 2^c, c chosen
+// per (column, block) so the block's largest magnitude lands in [2^14,
+// 2^15); the factor 2^-c goes to fx. Multiplying by a power of two is exact,
+// and a bf16 value (8 significant bits) is exact in f16 when the result is
+// at least 2^-17, i.e. for every element within 2^31 of its block maximum.
+
+// Floor of log2 of a positive float given its bit pattern (no sign).
+__device__ __forceinline__ int floor_log2_f32_bits(uint32_t a) {
+    const int e = static_cast<int>(a >> 23);
+    return e ? e - 127 : (31 - __clz(static_cast<int>(a))) - 149;
+}
+
+// Scale exponent c for a block whose largest |value| has floor(log2) fl
+// (capped so the factor 2^-c stays a representable float).
+__device__ __forceinline__ int staging_exponent(int fl) { return min(14 - fl, 149); }
+
+// v * 2^c for c in [-149 + 14, 149 + 14] without overflow in the factor.
+struct Pow2Scaler {
+    float s1, s2;
+    bool two;
+    __device__ explicit Pow2Scaler(int c) {
+        two = c > 127 || c < -126;
+        const int c1 = two ? (c > 0 ? 64 : -64) : 0;
+        s1 = exp2_int(c - c1);
+        s2 = exp2_int(c1);
+    }
+    __device__ float operator()(float v) const { return two ? (v * s1) * s2 : v * s1; }
+};
+
+// Stage one block of 32 bf16 values (16 words) as f16 column data.
+__device__ __forceinline__ void stage_bf16_block(const uint32_t (&w)[16], uint8_t* dst, float* fx_out) {
+    uint32_t amax = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) amax = max(amax, max(w[j] & 0x7fffu, (w[j] >> 16) & 0x7fffu));
+    int c = 0;
+    if (amax != 0) c = staging_exponent(floor_log2_f32_bits(amax << 16));
+    const Pow2Scaler sc(c);
+    uint32_t o[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        __half2 h = __floats2half2_rn(sc(__uint_as_float(w[j] << 16)), sc(__uint_as_float(w[j] & 0xffff0000u)));
+        o[j] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) d[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+    *fx_out = exp2_int(-c);
+}
+
+// Stage one block of 32 fp32 values as an exact-to-22-bits pair of f16
+// columns: hi = f16(v * 2^c), lo = f16(v * 2^c - hi). Both share the factor.
+__device__ __forceinline__ void stage_f32_block_split(const float (&v)[32], uint8_t* dst_hi, uint8_t* dst_lo,
+                                                      float* fx_hi, float* fx_lo) {
+    uint32_t amax = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) amax = max(amax, __float_as_uint(v[j]) & 0x7fffffffu);
+    int c = 0;
+    if (amax != 0) c = staging_exponent(floor_log2_f32_bits(amax));
+    const Pow2Scaler sc(c);
+    uint32_t oh[16], ol[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const float a = sc(v[2 * j]);
+        const float b = sc(v[2 * j + 1]);
+        const __half2 hi = __floats2half2_rn(a, b);
+        const float2 hf = __half22float2(hi);
+        const __half2 lo = __floats2half2_rn(a - hf.x, b - hf.y);
+        oh[j] = *reinterpret_cast<const uint32_t*>(&hi);
+        ol[j] = *reinterpret_cast<const uint32_t*>(&lo);
+    }
+    uint4* dh = reinterpret_cast<uint4*>(dst_hi);
+    uint4* dl = reinterpret_cast<uint4*>(dst_lo);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        dh[q] = make_uint4(oh[4 * q], oh[4 * q + 1], oh[4 * q + 2], oh[4 * q + 3]);
+        dl[q] = make_uint4(ol[4 * q], ol[4 * q + 1], ol[4 * q + 2], ol[4 * q + 3]);
+    }
+    const float f = exp2_int(-c);
+    *fx_hi = f;
+    *fx_lo = f;
+}
+
+// ------------------------------------------------------------------------
+// One K step of one unit: BOXES boxes of 16 rows x 256 K (8 blocks of 32;
+// fewer at the end of K), against the staged columns. Blocks are numbered
+// globally (scales) and relative to kblk0 (staged activations).
+template <int NT, int BOXES>
+__device__ __forceinline__ void consume_step(uint32_t slot, const uint8_t* __restrict__ sc, int nblk, int kb,
+                                             int kblk0, int kblk1, int ncols, int xcols, const uint8_t* xs,
+                                             const float* fx, float (&acc)[BOXES][NT][4], int lane) {
+    const int g = lane >> 2;
+    const int tig = lane & 3;
+    const int mi = lane >> 3;
+    const int row = ((mi & 1) << 3) | (lane & 7);
+    const int bsel = mi >> 1;
+    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int jp = 0; jp < 4; ++jp) {
+        const int b_first = kb * 8 + 2 * jp;
+        if (b_first >= kblk1) break;
+        const uint32_t roff = row * 128 + (((2 * jp + bsel) ^ (row & 7)) << 4);
+        uint32_t r[BOXES][4];
+#pragma unroll
+        for (int bx = 0; bx < BOXES; ++bx)
+            ldmatrix_x4(slot + bx * kBoxBytes + roff, r[bx][0], r[bx][1], r[bx][2], r[bx][3]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int b = b_first + h;
+            if (b >= kblk1) break;
+            const int bl = b - kblk0;
+            uint4 xv[NT];
+            float2 f[NT];
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                const int col = g + 8 * n;
+                xv[n] = make_uint4(0, 0, 0, 0);
+                if (col < ncols)
+                    xv[n] = *reinterpret_cast<const uint4*>(xs + (size_t)(bl * xcols + col) * 64 + tig * 16);
+                f[n] = *reinterpret_cast<const float2*>(fx + bl * 8 * NT + 8 * n + 2 * tig);
+            }
+#pragma unroll
+            for (int bx = 0; bx < BOXES; ++bx) {
+                uint32_t ga[4], gb[4];
+                e2m1x8_to_f16x8(r[bx][2 * h], ga[0], ga[1], ga[2], ga[3]);
+                e2m1x8_to_f16x8(r[bx][2 * h + 1], gb[0], gb[1], gb[2], gb[3]);
+                const uint8_t* scb = sc + bx * 16 * nblk;
+                const float fw0 = e8m0_to_float(scb[g * nblk + b]);
+                const float fw1 = e8m0_to_float(scb[(g + 8) * nblk + b]);
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    float d[4];
+                    mma_f16_16816(d, ga[0], gb[0], ga[1], gb[1], xv[n].x, xv[n].y, zero4);
+                    mma_f16_16816(d, ga[2], gb[2], ga[3], gb[3], xv[n].z, xv[n].w, d);
+                    acc[bx][n][0] = fmaf(d[0], fw0 * f[n].x, acc[bx][n][0]);
+                    acc[bx][n][1] = fmaf(d[1], fw0 * f[n].y, acc[bx][n][1]);
+                    acc[bx][n][2] = fmaf(d[2], fw1 * f[n].x, acc[bx][n][2]);
+                    acc[bx][n][3] = fmaf(d[3], fw1 * f[n].y, acc[bx][n][3]);
+                }
+            }
+        }
+    }
+}
+
+// Final per-unit sums handed to a problem's epilogue: [box][column][16 rows].
+template <int NT>
+struct Sums {
+    const float* f;
+    __device__ float sum(int box, int col, int r) const { return f[(box * 8 * NT + col) * 16 + r]; }
+};
+
+// Where a CTA sits: which units, which part of K.
+struct Placement {
+    int u0, u1;        // units [u0, u1)
+    int kb0, kb1;      // K steps [kb0, kb1) (256 values each)
+    int kblk0, kblk1;  // 32-blocks [kblk0, kblk1)
+    uint32_t rank, cl;
+};
+
+// ------------------------------------------------------------------------
+// Shared-memory carve-up of one CTA (offsets from the 1024-aligned base).
+struct Smem {
+    uint32_t base;
+    uint8_t* gbase;
+    SmemLayout L;
+    Bars bars;
+    uint32_t cbars;  // cluster barriers: cfull[2], cempty[2]
+};
+
+template <class P>
+__device__ void producer_role(const typename P::Params& p, const Smem& S, const Placement& pl,
+                              const CUtensorMap* tmap, int lane) {
+    constexpr int BOXES = P::BOXES;
+    constexpr uint32_t kSlotBytes = BOXES * kBoxBytes;
+    const SmemLayout& L = S.L;
+    const Bars& bars = S.bars;
+    const uint32_t scale_bytes = 16u * static_cast<uint32_t>(p.nblk);
+    const uint64_t policy = l2_evict_first_policy();
+    bool ok = true;
+    uint32_t issued = 0, sissued = 0;
+    for (int u = pl.u0; u < pl.u1 && ok; ++u) {
+        const uint32_t uu = u - pl.u0;
+        const uint32_t ss = uu % L.nss;
+        if (lane == 0) ok = mbar_wait(bars.sempty(ss), ((uu / L.nss) & 1) ^ 1, p.status);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        const uint32_t bytes = static_cast<uint32_t>(P::unit_rows(p, u)) * static_cast<uint32_t>(p.nblk);
+        const uint32_t dst = S.base + L.sc + ss * L.ss_bytes;
+        if ((bytes & 15u) == 0) {
+            if (lane == 0) {
+                mbar_arrive_expect_tx(bars.sfull(ss), bytes * BOXES);
+#pragma unroll
+                for (int bx = 0; bx < BOXES; ++bx)
+                    bulk_load(dst + bx * scale_bytes, P::scale_src(p, u, bx), bytes, bars.sfull(ss), policy);
+            }
+        } else {
+            uint8_t* d = S.gbase + L.sc + ss * L.ss_bytes;
+#pragma unroll
+            for (int bx = 0; bx < BOXES; ++bx) {
+                const uint8_t* src = P::scale_src(p, u, bx);
+                for (uint32_t b = lane; b < bytes; b += 32) d[bx * scale_bytes + b] = src[b];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.sfull(ss));
+        }
+        ++sissued;
+        int rows[BOXES];
+#pragma unroll
+        for (int bx = 0; bx < BOXES; ++bx) rows[bx] = P::box_row(p, u, bx);
+        for (int kb = pl.kb0; kb < pl.kb1; ++kb) {
+            const uint32_t slot = issued % L.nslot;
+            const uint32_t ph = (issued / L.nslot) & 1;
+            if (lane == 0) {
+                ok = mbar_wait(bars.empty(slot), ph ^ 1, p.status);
+                if (ok) {
+                    mbar_arrive_expect_tx(bars.full(slot), kSlotBytes);
+#pragma unroll
+                    for (int bx = 0; bx < BOXES; ++bx)
+                        tma_load_2d(S.base + L.ring + slot * kSlotBytes + bx * kBoxBytes, tmap, kb * 128, rows[bx],
+                                    bars.full(slot), policy);
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            ++issued;
+        }
+    }
+    if (!ok && lane == 0) {
+        // Let every copy still in flight land (bounded) before the CTA exits.
+        const uint32_t first = issued > L.nslot ? issued - L.nslot : 0;
+        for (uint32_t j = first; j < issued; ++j) mbar_wait(bars.full(j % L.nslot), (j / L.nslot) & 1, p.status);
+        const uint32_t sfirst = sissued > L.nss ? sissued - L.nss : 0;
+        for (uint32_t j = sfirst; j < sissued; ++j) mbar_wait(bars.sfull(j % L.nss), (j / L.nss) & 1, p.status);
+    }
+}
+
+template <class P>
+__device__ void consumer_role(const typename P::Params& p, const Smem& S, const Placement& pl, int warp, int lane) {
+    constexpr int NT = P::NT;
+    constexpr int BOXES = P::BOXES;
+    constexpr uint32_t kSlotBytes = BOXES * kBoxBytes;
+    constexpr int kRedWarpFloats = BOXES * 8 * NT * kRedStride;
+    const SmemLayout& L = S.L;
+    const Bars& bars = S.bars;
+    uint8_t* xs = S.gbase + L.xs;
+    float* fx = reinterpret_cast<float*>(S.gbase + L.fx);
+    float* redw = reinterpret_cast<float*>(S.gbase + L.red);
+    const uint8_t* scb = S.gbase + L.sc;
+    const int nkbc = pl.kb1 - pl.kb0;
+    int cur_chunk = -1;
+    int ncols = 0;
+    uint32_t i = warp;
+    for (int u = pl.u0; u < pl.u1; ++u) {
+        const uint32_t uu = u - pl.u0;
+        const int chunk = P::chunk_of(p, u);
+        if (chunk != cur_chunk) {
+            // Everyone is done with the previous columns before they change.
+            named_barrier_sync(1, kConsumerThreads);
+            P::stage(p, chunk, pl.kblk0, pl.kblk1, xs, fx, warp * 32 + lane, kConsumerThreads);
+            named_barrier_sync(1, kConsumerThreads);
+            cur_chunk = chunk;
+            ncols = P::ncols(p, chunk);
+        }
+        const uint32_t ss = uu % L.nss;
+        if (!warp_wait(bars.sfull(ss), (uu / L.nss) & 1, p.status)) return;
+        const uint8_t* sc = scb + ss * L.ss_bytes;
+        float acc[BOXES][NT][4];
+#pragma unroll
+        for (int bx = 0; bx < BOXES; ++bx)
+#pragma unroll
+            for (int n = 0; n < NT; ++n) acc[bx][n][0] = acc[bx][n][1] = acc[bx][n][2] = acc[bx][n][3] = 0.f;
+        const uint32_t ib = uu * nkbc;
+        for (; i < ib + nkbc; i += kConsumerWarps) {
+            const uint32_t slot = i % L.nslot;
+            if (!warp_wait(bars.full(slot), (i / L.nslot) & 1, p.status)) return;
+            consume_step<NT, BOXES>(S.base + L.ring + slot * kSlotBytes, sc, p.nblk, pl.kb0 + static_cast<int>(i - ib),
+                                    pl.kblk0, pl.kblk1, ncols, p.xcols, xs, fx, acc, lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.empty(slot));
+        }
+        const uint32_t rb = uu & 1;
+        if (!warp_wait(bars.rempty(rb), ((uu >> 1) & 1) ^ 1, p.status)) return;
+        float* R = redw + (rb * kConsumerWarps + warp) * kRedWarpFloats;
+        const int g = lane >> 2, tig = lane & 3;
+#pragma unroll
+        for (int bx = 0; bx < BOXES; ++bx)
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                float* Rb = R + (bx * 8 * NT + 8 * n + 2 * tig) * kRedStride;
+                Rb[g] = acc[bx][n][0];
+                Rb[kRedStride + g] = acc[bx][n][1];
+                Rb[g + 8] = acc[bx][n][2];
+                Rb[kRedStride + g + 8] = acc[bx][n][3];
+            }
+        __syncwarp();
+        if (lane == 0) {
+            mbar_arrive(bars.rfull(rb));
+            mbar_arrive(bars.sempty(ss));
+        }
+    }
+}
+
+template <class P>
+__device__ void reducer_role(const typename P::Params& p, const Smem& S, const Placement& pl, int lane) {
+    constexpr int NT = P::NT;
+    constexpr int BOXES = P::BOXES;
+    constexpr int kRedWarpFloats = BOXES * 8 * NT * kRedStride;
+    constexpr int kFin = BOXES * 8 * NT * 16;  // floats of one unit's sums
+    const SmemLayout& L = S.L;
+    const Bars& bars = S.bars;
+    const float* red = reinterpret_cast<const float*>(S.gbase + L.red);
+    float* fin = reinterpret_cast<float*>(S.gbase + L.fin);
+    const float* recv = reinterpret_cast<const float*>(S.gbase + L.recv);
+    const uint32_t cfull0 = S.cbars, cempty0 = S.cbars + 16;
+    for (int u = pl.u0; u < pl.u1; ++u) {
+        const uint32_t uu = u - pl.u0;
+        const uint32_t rb = uu & 1;
+        if (!warp_wait(bars.rfull(rb), (uu >> 1) & 1, p.status)) return;
+        const int ncols = P::ncols(p, P::chunk_of(p, u));
+        // CTA-local sums over the consumer warps, fixed order.
+        const float* R = red + rb * kConsumerWarps * kRedWarpFloats;
+        float* F = fin + rb * kFin;
+        for (int e = lane; e < BOXES * ncols * 16; e += 32) {
+            const int bx = e / (ncols * 16);
+            const int rem = e - bx * ncols * 16;
+            const int col = rem >> 4, r = rem & 15;
+            float s = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) s += R[w * kRedWarpFloats + (bx * 8 * NT + col) * kRedStride + r];
+            F[(bx * 8 * NT + col) * 16 + r] = s;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.rempty(rb));
+        if (pl.cl > 1) {
+            if (pl.rank != 0) {
+                // Send this CTA's part of K to the leader, in its rank's slot.
+                if (!__all_sync(0xffffffffu, mbar_wait_cluster(cempty0 + 8 * rb, ((uu >> 1) & 1) ^ 1, p.status)))
+                    return;
+                const uint32_t dst = map_to_rank(S.base + L.recv + ((rb * (pl.cl - 1) + pl.rank - 1) * kFin) * 4, 0);
+                for (int e = lane; e < BOXES * ncols * 16; e += 32) {
+                    const int bx = e / (ncols * 16);
+                    const int rem = e - bx * ncols * 16;
+                    const int idx = (bx * 8 * NT + (rem >> 4)) * 16 + (rem & 15);
+                    st_cluster_f32(dst + idx * 4, F[idx]);
+                }
+                mbar_arrive_remote(map_to_rank(cfull0 + 8 * rb, 0));
+                continue;
+            }
+            // Leader: add the other ranks' parts in rank order.
+            if (!__all_sync(0xffffffffu, mbar_wait_cluster(cfull0 + 8 * rb, (uu >> 1) & 1, p.status))) return;
+            for (int e = lane; e < BOXES * ncols * 16; e += 32) {
+                const int bx = e / (ncols * 16);
+                const int rem = e - bx * ncols * 16;
+                const int idx = (bx * 8 * NT + (rem >> 4)) * 16 + (rem & 15);
+                float s = F[idx];
+                for (uint32_t q = 0; q + 1 < pl.cl; ++q) s += recv[(rb * (pl.cl - 1) + q) * kFin + idx];
+                F[idx] = s;
+            }
+            __syncwarp();
+            for (uint32_t q = 1; q < pl.cl; ++q) mbar_arrive_remote(map_to_rank(cempty0 + 8 * rb, q));
+        }
+        P::epilogue(p, u, Sums<NT>{F}, lane);
+        __syncwarp();
+    }
+}
+
+// ------------------------------------------------------------------------
+// The kernel. P (the problem) supplies:
+//   static constexpr int NT, BOXES;
+//   struct Params { ...; unsigned* status; int nblk; int nkb; int xcols; int cl; SmemLayout layout; };
+//     xcols = staged columns per block: xs[block][xcols][32] f16, fx[block][8*NT] f32
+//     (zero factors for unused columns); cl = CTAs per cluster splitting K.
+//   __device__ static int  num_units(const Params&);
+//   __device__ static int  chunk_of(const Params&, int u);
+//   __device__ static int  box_row(const Params&, int u, int box);      // TMA row coordinate
+//   __device__ static const uint8_t* scale_src(const Params&, int u, int box);
+//   __device__ static int  unit_rows(const Params&, int u);            // valid rows (<= 16)
+//   __device__ static int  ncols(const Params&, int chunk);            // staged columns
+//   __device__ static void stage(const Params&, int chunk, int kblk0, int kblk1, uint8_t* xs, float* fx,
+//                                int tid, int nthreads);
+//   __device__ static void epilogue(const Params&, int u, const Sums<NT>&, int lane);
+template <class P>
+__global__ void __launch_bounds__(kThreads, 1)
+    stream_kernel(const __grid_constant__ CUtensorMap tmap, const typename P::Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    Smem S;
+    S.base = (raw + 1023u) & ~1023u;
+    S.gbase = smem_raw + (S.base - raw);
+    S.L = p.layout;
+    S.bars = Bars{S.base + S.L.bars, S.L.nslot, S.L.nss};
+    S.cbars = S.base + S.L.bars + 8 * (2 * S.L.nslot + 2 * S.L.nss + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    Placement pl;
+    pl.cl = p.cl > 1 ? static_cast<uint32_t>(p.cl) : 1u;
+    pl.rank = pl.cl > 1 ? cluster_ctarank() : 0u;
+    const int ngroups = pl.cl > 1 ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
+    const int group = pl.cl > 1 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+    const int nkb_c = (p.nkb + static_cast<int>(pl.cl) - 1) / static_cast<int>(pl.cl);
+    pl.kb0 = min(p.nkb, static_cast<int>(pl.rank) * nkb_c);
+    pl.kb1 = min(p.nkb, pl.kb0 + nkb_c);
+    pl.kblk0 = pl.kb0 * 8;
+    pl.kblk1 = min(p.nblk, pl.kb1 * 8);
+
+    if (threadIdx.x == 0) {
+        const Bars& bars = S.bars;
+        for (uint32_t s = 0; s < S.L.nslot; ++s) {
+            mbar_init(bars.full(s), 1);
+            mbar_init(bars.empty(s), 1);
+        }
+        for (uint32_t s = 0; s < S.L.nss; ++s) {
+            mbar_init(bars.sfull(s), 1);
+            mbar_init(bars.sempty(s), kConsumerWarps);
+        }
+        for (uint32_t b = 0; b < 2; ++b) {
+            mbar_init(bars.rfull(b), kConsumerWarps);
+            mbar_init(bars.rempty(b), 1);
+            mbar_init(S.cbars + 8 * b, pl.cl > 1 ? 32 * (pl.cl - 1) : 1);  // cfull
+            mbar_init(S.cbars + 16 + 8 * b, 32);                          // cempty
+        }
+        fence_barrier_init();
+    }
+    if (pl.cl > 1)
+        cluster_sync_all();
+    else
+        __syncthreads();
+
+    const int U = P::num_units(p);
+    pl.u0 = static_cast<int>((int64_t)U * group / ngroups);
+    pl.u1 = static_cast<int>((int64_t)U * (group + 1) / ngroups);
+
+    if (warp == kProducerWarp)
+        producer_role<P>(p, S, pl, &tmap, lane);
+    else if (warp == kReducerWarp)
+        reducer_role<P>(p, S, pl, lane);
+    else
+        consumer_role<P>(p, S, pl, warp, lane);
+
+    // No CTA of a cluster leaves while another may still write to it.
+    if (pl.cl > 1) cluster_sync_all();
+}
+
+// Host launcher: one CTA per SM (or clusters of p.cl CTAs), never more
+// groups than units.
+template <class Prob>
+cudaError_t launch_stream_kernel(const CUtensorMap& tmap, const typename Prob::Params& p, int units, int num_sms,
+                                 cudaStream_t stream) {
+    static int configured[64] = {0};  // dynamic smem already allowed, per device
+    static int clusters_cached[64][9] = {};  // co-resident clusters per device and size
+    const int smem = static_cast<int>(p.layout.total) + 1024;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64 || configured[dev] < smem) {
+        cudaError_t e = cudaFuncSetAttribute(stream_kernel<Prob>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 64) configured[dev] = smem;
+    }
+    const int cl = p.cl > 1 ? p.cl : 1;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    int groups = num_sms;
+    if (cl > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = cl;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cfg.gridDim = dim3(cl * (num_sms / cl));
+        int nclusters = (dev >= 0 && dev < 64 && cl <= 8) ? clusters_cached[dev][cl] : 0;
+        if (nclusters == 0) {
+            cudaError_t e = cudaOccupancyMaxActiveClusters(&nclusters, stream_kernel<Prob>, &cfg);
+            if (e != cudaSuccess) return e;
+            if (nclusters < 1) return cudaErrorInvalidConfiguration;
+            if (dev >= 0 && dev < 64 && cl <= 8) clusters_cached[dev][cl] = nclusters;
+        }
+        groups = nclusters;
+    }
+    if (groups > units) groups = units;
+    if (groups < 1) groups = 1;
+    cfg.gridDim = dim3(groups * cl);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, stream_kernel<Prob>, tmap, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace mxfp4

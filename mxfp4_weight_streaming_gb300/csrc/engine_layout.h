@@ -1,0 +1,74 @@
+// Shared-memory plan of one weight-streaming CTA (host and device view).
+#pragma once
+
+#include <stdint.h>
+
+namespace mxfp4 {
+
+// Byte offsets inside the 1024-aligned dynamic shared memory of one CTA.
+struct SmemLayout {
+    uint32_t ring;      // weight ring: nslot slots of BOXES x 2048 bytes
+    uint32_t nslot;
+    uint32_t xs;        // staged activations, f16 [blocks][xcols][32]
+    uint32_t fx;        // activation block factors, f32 [blocks][8*NT]
+    uint32_t sc;        // scale ring: nss slots of ss_bytes
+    uint32_t nss;
+    uint32_t ss_bytes;  // one unit's scales: BOXES x 16 x K/32 bytes
+    uint32_t red;       // double-buffered reduction area (per consumer warp)
+    uint32_t fin;       // double-buffered per-unit sums of this CTA
+    uint32_t recv;      // cluster leader: the other ranks' sums, [2][cl-1]
+    uint32_t bars;      // mbarriers (ring, scales, reduction, cluster)
+    uint32_t total;
+};
+
+// Picks the deepest weight ring (<= 64 slots) that fits next to the staged
+// activations; the scale ring is deep enough that the producer is never held
+// back by it. Returns false if not even a 16-slot ring fits.
+// nblk is the number of 32-blocks this CTA stages (its part of K); nblk_all
+// is the whole row's count (scales cover all of K).
+inline bool plan_layout(int nt, int boxes, int nblk, int nblk_all, int xcols, int cl, int consumer_warps,
+                        int red_stride, int max_smem, SmemLayout* out) {
+    auto al = [](uint32_t v, uint32_t a) { return (v + a - 1) / a * a; };
+    const int nkb = (nblk + 7) / 8;
+    const uint32_t slot_bytes = 2048u * boxes;
+    const uint32_t xs_bytes = al(static_cast<uint32_t>(nblk) * xcols * 64, 16);
+    const uint32_t fx_bytes = al(static_cast<uint32_t>(nblk) * 8 * nt * 4, 16);
+    const uint32_t ss_bytes = al(static_cast<uint32_t>(boxes) * 16 * nblk_all, 16);
+    const uint32_t red_bytes = 2u * consumer_warps * boxes * 8 * nt * red_stride * 4;
+    const uint32_t fin_bytes = 2u * boxes * 8 * nt * 16 * 4;
+    const uint32_t recv_bytes = cl > 1 ? fin_bytes * (cl - 1) : 0;
+    const int budget = max_smem - 1024;
+    for (int nslot = 64 / boxes; nslot >= 16 / boxes; --nslot) {
+        int nss = (nslot + nkb - 1) / nkb + 1;
+        nss = nss < 2 ? 2 : (nss > 16 ? 16 : nss);
+        SmemLayout l{};
+        uint32_t off = 0;
+        l.ring = off;
+        l.nslot = nslot;
+        off += nslot * slot_bytes;
+        l.xs = off;
+        off += xs_bytes;
+        l.fx = off;
+        off += fx_bytes;
+        l.sc = off;
+        l.nss = nss;
+        l.ss_bytes = ss_bytes;
+        off += nss * ss_bytes;
+        l.red = off;
+        off += red_bytes;
+        l.fin = off;
+        off += fin_bytes;
+        l.recv = off;
+        off += recv_bytes;
+        l.bars = al(off, 8);
+        off = l.bars + 8 * (2 * nslot + 2 * nss + 4 + 4);
+        l.total = off;
+        if (static_cast<int>(off) <= budget) {
+            *out = l;
+            return true;
+        }
+    }
+    return false;
+}
+
+}  // namespace mxfp4

@@ -1,0 +1,91 @@
+// Weight-streaming MXFP4 linear layer for sm_103a (dense and LM-head shapes).
+//
+// What it computes ("Zyphra Inference Wave 2", section "Speculative
+// decoding"; AMD "megakernel-intro", section "3. Low-Precision Data Types"):
+//   y[t][n] = bf16( sum_k x[t][k] * w[n][k] ),  w = e2m1(code) * 2^(s-127)
+// for the handful of tokens t of one decode / verify step, reading every
+// weight byte from HBM once. A unit is 16 output rows over all of K; the T
+// tokens are staged once per CTA (see engine.cuh).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "engine.cuh"
+#include "linear_launch.h"
+
+namespace mxfp4 {
+
+template <int NT_>
+struct DenseProblem {
+    static constexpr int NT = NT_;
+    static constexpr int BOXES = 1;
+    using Params = LinearParams;
+
+    __device__ static int num_units(const Params& p) { return p.n_rg; }
+    __device__ static int chunk_of(const Params&, int) { return 0; }
+    __device__ static int box_row(const Params&, int u, int) { return u * 16; }
+    __device__ static const uint8_t* scale_src(const Params& p, int u, int) {
+        return p.ws + (size_t)u * 16 * p.nblk;
+    }
+    __device__ static int unit_rows(const Params& p, int u) { return min(16, p.N - u * 16); }
+    __device__ static int ncols(const Params& p, int) { return p.T; }
+
+    __device__ static void stage(const Params& p, int, int kblk0, int kblk1, uint8_t* xs, float* fx, int tid,
+                                 int nthreads) {
+        const int T = p.T;
+        const int nb = kblk1 - kblk0;
+        const int items = nb * T;
+        for (int it = tid; it < items; it += nthreads) {
+            const int b = it / T;
+            const int t = it - b * T;
+            const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * p.K + (size_t)(kblk0 + b) * 32);
+            uint4 v[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) v[q] = __ldg(src + q);
+            const uint32_t w[16] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w,
+                                    v[2].x, v[2].y, v[2].z, v[2].w, v[3].x, v[3].y, v[3].z, v[3].w};
+            stage_bf16_block(w, xs + (size_t)(b * p.xcols + t) * 64, fx + b * 8 * NT + t);
+        }
+        for (int it = tid; it < nb * 8 * NT; it += nthreads)
+            if (it % (8 * NT) >= T) fx[it] = 0.0f;
+    }
+
+    __device__ static void epilogue(const Params& p, int u, const Sums<NT>& v, int lane) {
+        for (int e = lane; e < p.T * 16; e += 32) {
+            const int t = e >> 4;
+            const int r = e & 15;
+            const float s = v.sum(0, t, r);
+            const int row = u * 16 + r;
+            if (row < p.N) p.y[(size_t)t * p.N + row] = __float2bfloat16_rn(s);
+        }
+    }
+};
+
+static int tokens_to_nt(int T) { return T <= 8 ? 1 : (T <= 16 ? 2 : 4); }
+
+bool plan_linear(int T, int K, int max_smem, int* cl, SmemLayout* L) {
+    const int nblk = K / 32;
+    const int nkb = (K + 255) / 256;
+    for (int c = 1; c <= 8; c *= 2) {
+        if (c > 1 && c > nkb) break;
+        const int nkb_c = (nkb + c - 1) / c;
+        const int nb_local = nkb_c * 8 < nblk ? nkb_c * 8 : nblk;
+        if (plan_layout(tokens_to_nt(T), 1, nb_local, nblk, T, c, kConsumerWarps, kRedStride, max_smem, L)) {
+            *cl = c;
+            return true;
+        }
+    }
+    return false;
+}
+
+cudaError_t launch_linear(const CUtensorMap& tmap, const LinearParams& p, int num_sms, cudaStream_t stream) {
+    switch (tokens_to_nt(p.T)) {
+        case 1: return launch_stream_kernel<DenseProblem<1>>(tmap, p, p.n_rg, num_sms, stream);
+        case 2: return launch_stream_kernel<DenseProblem<2>>(tmap, p, p.n_rg, num_sms, stream);
+        default: return launch_stream_kernel<DenseProblem<4>>(tmap, p, p.n_rg, num_sms, stream);
+    }
+}
+
+}  // namespace mxfp4

@@ -1,0 +1,28 @@
+// Host/device interface of the grouped top-k MoE kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mxfp4 {
+
+struct MoeArgs {
+    const __nv_bfloat16* x;  // [T][hidden]
+    const float* logits;     // [T][E]
+    const uint8_t *w1q, *w1s, *w2q, *w2s;
+    __nv_bfloat16* y;        // [T][hidden]
+    int32_t* topk_ids;       // optional [T][top_k]
+    float* topk_w;           // optional [T][top_k]
+    void* workspace;
+    unsigned* status;
+    int T, E, top_k, hidden, inter;
+};
+
+size_t moe_workspace_bytes(int64_t t, int64_t e, int top_k, int64_t hidden, int64_t inter);
+int launch_moe(const CUtensorMap& map1, const CUtensorMap& map2, const MoeArgs& a, int num_sms, int max_smem,
+               cudaStream_t stream);
+
+}  // namespace mxfp4

@@ -1,0 +1,71 @@
+"""The C-ABI library builds, loads on a machine without a GPU, exports every
+function include/mxfp4.h declares, and rejects bad arguments before any
+launch (these calls need no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from mxfp4_weight_streaming_gb300 import build
+    import mxfp4_weight_streaming_gb300 as mx
+    build.build()
+    return mx.load()
+
+
+def declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"\b(mxfp4_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert "mxfp4_linear" in names and "mxfp4_moe" in names and "mxfp4_quantize" in names
+    for name in names:
+        assert hasattr(L, name), name
+
+
+def test_strerror(L):
+    import mxfp4_weight_streaming_gb300 as mx
+    for code in range(7):
+        assert mx.strerror(code).startswith("MXFP4")
+    assert "unknown" in mx.strerror(99)
+
+
+def test_argument_errors_return_before_launch(L):
+    import mxfp4_weight_streaming_gb300 as mx
+    p = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+    odd = ctypes.c_void_p(0x1001)
+    assert mx.mxfp4_linear(None, 1, 64, p, p, 8, p, None) == mx.MXFP4_ERR_INVALID_ARG
+    assert mx.mxfp4_linear(p, 0, 64, p, p, 8, p, None) == mx.MXFP4_ERR_INVALID_ARG
+    assert mx.mxfp4_linear(p, 1, 48, p, p, 8, p, None) == mx.MXFP4_ERR_SHAPE
+    assert mx.mxfp4_linear(p, 33, 64, p, p, 8, p, None) == mx.MXFP4_ERR_SHAPE
+    assert mx.mxfp4_linear(odd, 1, 64, p, p, 8, p, None) == mx.MXFP4_ERR_ALIGN
+    assert mx.mxfp4_quantize(p, 4, 33, p, p, None) == mx.MXFP4_ERR_SHAPE
+    assert mx.mxfp4_quantize(None, 4, 32, p, p, None) == mx.MXFP4_ERR_INVALID_ARG
+    args = dict(t=4, hidden=64, e=8, top_k=2, inter=64)
+    base = [p, args["t"], args["hidden"], p, args["e"], args["top_k"], p, p, p, p, args["inter"], p, None, None,
+            p, 1 << 30, None]
+    bad = list(base)
+    bad[5] = 9  # top_k > e
+    assert mx.mxfp4_moe(*bad) == mx.MXFP4_ERR_SHAPE
+    bad = list(base)
+    bad[14] = None  # no workspace
+    assert mx.mxfp4_moe(*bad) == mx.MXFP4_ERR_WORKSPACE
+    bad = list(base)
+    bad[15] = 16  # workspace too small
+    assert mx.mxfp4_moe(*bad) == mx.MXFP4_ERR_WORKSPACE
+    bad = list(base)
+    bad[2] = 48  # hidden % 32
+    assert mx.mxfp4_moe(*bad) == mx.MXFP4_ERR_SHAPE
+    assert mx.mxfp4_moe_workspace_size(32, 256, 8, 7168, 2048) > 0

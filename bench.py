@@ -48,6 +48,8 @@ WORKLOADS = {
     "ffn_up_t32_k7168_n18432": dict(t=32, k=7168, n=18432, seed=3, x64=False),
 }
 DEFAULT_WORKLOAD = "verify_t4_k7168_n7168"
+MOE_WORKLOAD = "moe_e256_top8_t32"
+MOE = dict(t=32, e=256, top_k=8, hidden=7168, inter=2048, seed=4)
 
 
 def algorithmic_bytes(t: int, k: int, n: int) -> int:
@@ -339,6 +341,71 @@ def run_ours(args, wl_name: str, rank: int, world: int, device, with_cpu_baselin
     return res
 
 
+# ------------------------------------------------------------- MoE arm
+def moe_expert_bytes(hidden: int, inter: int) -> int:
+    return 2 * inter * (hidden // 2 + hidden // 32) + hidden * (inter // 2 + inter // 32)
+
+
+def run_moe(steps: int, warmup: int, device):
+    """Grouped top-8 MoE decode step (256 experts, T=32): one mxfp4_moe call
+    per step; bytes = distinct routed experts' W1+W2 (+ x, logits, y)."""
+    import torch
+
+    import mxfp4_weight_streaming_gb300 as mx
+    import synth
+
+    m = MOE
+    t, e, top_k, hidden, inter, seed = m["t"], m["e"], m["top_k"], m["hidden"], m["inter"], m["seed"]
+    w1q = torch.empty((e, 2 * inter, hidden // 2), dtype=torch.uint8, device=device)
+    w1s = torch.empty((e, 2 * inter, hidden // 32), dtype=torch.uint8, device=device)
+    w2q = torch.empty((e, hidden, inter // 2), dtype=torch.uint8, device=device)
+    w2s = torch.empty((e, hidden, inter // 32), dtype=torch.uint8, device=device)
+    for ex in range(e):
+        a = synth.weights(seed, 2 * inter, hidden, device=device, row0=ex * 2 * inter)
+        q, sc = mx.quantize(a)
+        w1q[ex].copy_(q.view(2 * inter, -1))
+        w1s[ex].copy_(sc.view(2 * inter, -1))
+        b = synth.weights(seed, hidden, inter, tid=synth.TID_W2, device=device, row0=ex * hidden)
+        q, sc = mx.quantize(b)
+        w2q[ex].copy_(q.view(hidden, -1))
+        w2s[ex].copy_(sc.view(hidden, -1))
+        del a, b
+    x = synth.tokens(seed, t, hidden, device=device)
+    lg = synth.logits(seed, t, e, device=device)
+    distinct = int(torch.unique(torch.topk(lg.cpu(), top_k, dim=1).indices).numel())
+    ws = mx.moe_workspace(t, e, top_k, hidden, inter, device)
+    y = torch.empty((t, hidden), dtype=torch.bfloat16, device=device)
+    stream = torch.cuda.Stream(device)
+    lib = mx.load()
+    args = [x.data_ptr(), t, hidden, lg.data_ptr(), e, top_k, w1q.data_ptr(), w1s.data_ptr(), w2q.data_ptr(),
+            w2s.data_ptr(), inter, y.data_ptr(), None, None, ws.data_ptr(), ws.numel(), stream.cuda_stream]
+
+    def call():
+        rc = lib.mxfp4_moe(*args)
+        if rc != 0:
+            raise RuntimeError(mx.strerror(rc))
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, warmup)):
+            call()
+    stream.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            call()
+        end.record(stream)
+    end.synchronize()
+    ms = start.elapsed_time(end) / steps
+    nbytes = distinct * moe_expert_bytes(hidden, inter) + 2 * t * hidden + 4 * t * e + 2 * t * hidden
+    peak, _ = hbm_peak()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"us_per_call": round(ms * 1e3, 2), "GBps": round(gbs, 1), "pct_of_peak": round(100 * gbs / peak, 2),
+            "distinct_experts": distinct, "bytes_per_call": nbytes, "gpu_launches_per_call": 4,
+            "timing": "eager launches (4 kernels per call), device events"}
+
+
 # ------------------------------------------------------- CPU oracle timing
 def cpu_baseline(wl_name: str, budget_s: float = 12.0):
     """The oracle, as it stands, on this host's cores, on a bounded sample:
@@ -453,6 +520,11 @@ def main():
             except Exception as ex:  # report, do not hide
                 sweep[name] = {"error": str(ex)[:200]}
             torch.cuda.empty_cache()
+        try:
+            sweep[MOE_WORKLOAD] = run_moe(min(args.steps, 200), 5, device)
+        except Exception as ex:
+            sweep[MOE_WORKLOAD] = {"error": str(ex)[:200]}
+        torch.cuda.empty_cache()
         res["sweep"] = sweep
     if world > 1:
         torch.distributed.destroy_process_group()

@@ -54,17 +54,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Where a bounded wait reports: the per-device status word, and a per-CTA
+// abort flag in shared memory. Once one wait of a CTA has given up, every
+// later wait of that CTA fails at once, so the CTA winds down in one limit
+// rather than one limit per remaining wait.
+struct WaitCtx {
+    unsigned* status;
+    volatile int* abort;
+};
+
+__device__ __forceinline__ void record_timeout(const WaitCtx& w) {
+    *w.abort = 1;
+    atomicOr(w.status, kStatusTimeout);
+}
+
 // Waits until the phase with the given parity has completed. Returns false
-// (and records a timeout in *status) if that takes longer than the limit.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned* status) {
+// if the CTA has aborted or the wait takes longer than the limit.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtx& w) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
+        if (*w.abort) return false;
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (global_timer_ns() - t0 > kWaitLimitNs) {
-            atomicOr(status, kStatusTimeout);
+            record_timeout(w);
             return false;
         }
     }
@@ -118,15 +133,16 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 }
 
 // Bounded wait on a local mbarrier that other CTAs of the cluster arrive on.
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, unsigned* status) {
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, const WaitCtx& w) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
+        if (*w.abort) return false;
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait_cluster(bar, parity)) return true;
         if (global_timer_ns() - t0 > kWaitLimitNs) {
-            atomicOr(status, kStatusTimeout);
+            record_timeout(w);
             return false;
         }
     }
@@ -164,6 +180,34 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
+// ---------------------------------------------------- shared-memory loads
+// Explicit ld.shared on 32-bit shared addresses (a generic pointer into
+// shared memory would go through the slower generic path). Volatile so they
+// stay ordered after the mbarrier waits that publish the data.
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ float2 lds64f(uint32_t a) {
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t lds_u8(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+
 // ------------------------------------------------------- warp-level math
 // Four 8x8 b16 matrices from shared memory (lane l supplies the row address
 // of matrix l/8, row l%8); lane l receives 4 bytes of row l/4 of each.
@@ -176,7 +220,7 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_
 // D = A(16x16 f16) * B(16x8 f16) + C, fp32 accumulate.
 __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                               uint32_t b0, uint32_t b1, const float (&c)[4]) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%10,%11,%12,%13};"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])

@@ -35,11 +35,15 @@
 
 namespace mxfp4 {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kReducerWarp = kConsumerWarps;
-constexpr int kProducerWarp = kConsumerWarps + 1;
-constexpr int kThreads = (kConsumerWarps + 2) * 32;
-constexpr int kConsumerThreads = kConsumerWarps * 32;
+// Warps of a CTA: P::NCW consumers, then the reducer, then the producer.
+template <class P>
+struct Roles {
+    static constexpr int kConsumers = P::NCW;
+    static constexpr int kReducer = P::NCW;
+    static constexpr int kProducer = P::NCW + 1;
+    static constexpr int kThreads = (P::NCW + 2) * 32;
+    static constexpr int kConsumerThreads = P::NCW * 32;
+};
 constexpr int kBoxBytes = 2048;  // 16 rows x 128 bytes = 16 rows x 256 K values
 constexpr int kRedStride = 20;   // floats per column row of the reduction area (16 + 4 pad)
 
@@ -54,12 +58,8 @@ struct Bars {
     __device__ uint32_t rempty(uint32_t b) const { return base + 8 * (2 * nslot + 2 * nss + 2 + b); }
 };
 
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, unsigned* status) {
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
-}
-
-__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx& w) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, w));
 }
 
 // ------------------------------------------------------------------------
@@ -152,9 +152,9 @@ __device__ __forceinline__ void stage_f32_block_split(const float (&v)[32], uint
 // fewer at the end of K), against the staged columns. Blocks are numbered
 // globally (scales) and relative to kblk0 (staged activations).
 template <int NT, int BOXES>
-__device__ __forceinline__ void consume_step(uint32_t slot, const uint8_t* __restrict__ sc, int nblk, int kb,
-                                             int kblk0, int kblk1, int ncols, int xcols, const uint8_t* xs,
-                                             const float* fx, float (&acc)[BOXES][NT][4], int lane) {
+__device__ __forceinline__ void consume_step(uint32_t slot, uint32_t sc, int nblk, int kb, int kblk0, int kblk1,
+                                             int ncols, int xcols, uint32_t xs, uint32_t fx,
+                                             float (&acc)[BOXES][NT][4], int lane) {
     const int g = lane >> 2;
     const int tig = lane & 3;
     const int mi = lane >> 3;
@@ -181,18 +181,17 @@ __device__ __forceinline__ void consume_step(uint32_t slot, const uint8_t* __res
             for (int n = 0; n < NT; ++n) {
                 const int col = g + 8 * n;
                 xv[n] = make_uint4(0, 0, 0, 0);
-                if (col < ncols)
-                    xv[n] = *reinterpret_cast<const uint4*>(xs + (size_t)(bl * xcols + col) * 64 + tig * 16);
-                f[n] = *reinterpret_cast<const float2*>(fx + bl * 8 * NT + 8 * n + 2 * tig);
+                if (col < ncols) xv[n] = lds128(xs + (bl * xcols + col) * 64 + tig * 16);
+                f[n] = lds64f(fx + (bl * 8 * NT + 8 * n + 2 * tig) * 4);
             }
 #pragma unroll
             for (int bx = 0; bx < BOXES; ++bx) {
                 uint32_t ga[4], gb[4];
                 e2m1x8_to_f16x8(r[bx][2 * h], ga[0], ga[1], ga[2], ga[3]);
                 e2m1x8_to_f16x8(r[bx][2 * h + 1], gb[0], gb[1], gb[2], gb[3]);
-                const uint8_t* scb = sc + bx * 16 * nblk;
-                const float fw0 = e8m0_to_float(scb[g * nblk + b]);
-                const float fw1 = e8m0_to_float(scb[(g + 8) * nblk + b]);
+                const uint32_t scb = sc + bx * 16 * nblk;
+                const float fw0 = e8m0_to_float(lds_u8(scb + g * nblk + b));
+                const float fw1 = e8m0_to_float(lds_u8(scb + (g + 8) * nblk + b));
 #pragma unroll
                 for (int n = 0; n < NT; ++n) {
                     float d[4];
@@ -203,6 +202,71 @@ __device__ __forceinline__ void consume_step(uint32_t slot, const uint8_t* __res
                     acc[bx][n][2] = fmaf(d[2], fw1 * f[n].x, acc[bx][n][2]);
                     acc[bx][n][3] = fmaf(d[3], fw1 * f[n].y, acc[bx][n][3]);
                 }
+            }
+        }
+    }
+}
+
+// A full K step (all 8 blocks inside this CTA's range) with every shared
+// memory load of the step issued before the unpack / MMA chain, and the
+// scale bytes of 8 blocks read as one 8-byte word per row (needs K % 256
+// == 0 so the words are aligned).
+template <int NT, int BOXES>
+__device__ __forceinline__ void consume_step_full(uint32_t slot, uint32_t sc, int nblk, int kb, int kblk0, int ncols,
+                                                  int xcols, uint32_t xs, uint32_t fx, float (&acc)[BOXES][NT][4],
+                                                  int lane) {
+    const int g = lane >> 2;
+    const int tig = lane & 3;
+    const int mi = lane >> 3;
+    const int row = ((mi & 1) << 3) | (lane & 7);
+    const int bsel = mi >> 1;
+    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t r[BOXES][4][4];
+#pragma unroll
+    for (int bx = 0; bx < BOXES; ++bx)
+#pragma unroll
+        for (int jp = 0; jp < 4; ++jp)
+            ldmatrix_x4(slot + bx * kBoxBytes + row * 128 + (((2 * jp + bsel) ^ (row & 7)) << 4), r[bx][jp][0],
+                        r[bx][jp][1], r[bx][jp][2], r[bx][jp][3]);
+    uint2 s0[BOXES], s1[BOXES];
+#pragma unroll
+    for (int bx = 0; bx < BOXES; ++bx) {
+        const uint32_t scb = sc + bx * 16 * nblk + kb * 8;
+        s0[bx] = lds64(scb + g * nblk);
+        s1[bx] = lds64(scb + (g + 8) * nblk);
+    }
+    const int bl0 = kb * 8 - kblk0;
+#pragma unroll
+    for (int blk = 0; blk < 8; ++blk) {
+        const int bl = bl0 + blk;
+        uint4 xv[NT];
+        float2 f[NT];
+#pragma unroll
+        for (int n = 0; n < NT; ++n) {
+            const int col = g + 8 * n;
+            xv[n] = make_uint4(0, 0, 0, 0);
+            if (col < ncols) xv[n] = lds128(xs + (bl * xcols + col) * 64 + tig * 16);
+            f[n] = lds64f(fx + (bl * 8 * NT + 8 * n + 2 * tig) * 4);
+        }
+        const int jp = blk >> 1, h = blk & 1;
+#pragma unroll
+        for (int bx = 0; bx < BOXES; ++bx) {
+            const uint32_t w0 = blk < 4 ? s0[bx].x : s0[bx].y;
+            const uint32_t w1 = blk < 4 ? s1[bx].x : s1[bx].y;
+            const float fw0 = e8m0_to_float((w0 >> (8 * (blk & 3))) & 0xffu);
+            const float fw1 = e8m0_to_float((w1 >> (8 * (blk & 3))) & 0xffu);
+            uint32_t ga[4], gb[4];
+            e2m1x8_to_f16x8(r[bx][jp][2 * h], ga[0], ga[1], ga[2], ga[3]);
+            e2m1x8_to_f16x8(r[bx][jp][2 * h + 1], gb[0], gb[1], gb[2], gb[3]);
+#pragma unroll
+            for (int n = 0; n < NT; ++n) {
+                float d[4];
+                mma_f16_16816(d, ga[0], gb[0], ga[1], gb[1], xv[n].x, xv[n].y, zero4);
+                mma_f16_16816(d, ga[2], gb[2], ga[3], gb[3], xv[n].z, xv[n].w, d);
+                acc[bx][n][0] = fmaf(d[0], fw0 * f[n].x, acc[bx][n][0]);
+                acc[bx][n][1] = fmaf(d[1], fw0 * f[n].y, acc[bx][n][1]);
+                acc[bx][n][2] = fmaf(d[2], fw1 * f[n].x, acc[bx][n][2]);
+                acc[bx][n][3] = fmaf(d[3], fw1 * f[n].y, acc[bx][n][3]);
             }
         }
     }
@@ -231,6 +295,8 @@ struct Smem {
     SmemLayout L;
     Bars bars;
     uint32_t cbars;  // cluster barriers: cfull[2], cempty[2]
+    uint32_t xbars;  // consumer barriers around activation staging: [2]
+    WaitCtx wait;
 };
 
 template <class P>
@@ -247,7 +313,7 @@ __device__ void producer_role(const typename P::Params& p, const Smem& S, const 
     for (int u = pl.u0; u < pl.u1 && ok; ++u) {
         const uint32_t uu = u - pl.u0;
         const uint32_t ss = uu % L.nss;
-        if (lane == 0) ok = mbar_wait(bars.sempty(ss), ((uu / L.nss) & 1) ^ 1, p.status);
+        if (lane == 0) ok = mbar_wait(bars.sempty(ss), ((uu / L.nss) & 1) ^ 1, S.wait);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         const uint32_t bytes = static_cast<uint32_t>(P::unit_rows(p, u)) * static_cast<uint32_t>(p.nblk);
@@ -277,7 +343,7 @@ __device__ void producer_role(const typename P::Params& p, const Smem& S, const 
             const uint32_t slot = issued % L.nslot;
             const uint32_t ph = (issued / L.nslot) & 1;
             if (lane == 0) {
-                ok = mbar_wait(bars.empty(slot), ph ^ 1, p.status);
+                ok = mbar_wait(bars.empty(slot), ph ^ 1, S.wait);
                 if (ok) {
                     mbar_arrive_expect_tx(bars.full(slot), kSlotBytes);
 #pragma unroll
@@ -293,10 +359,13 @@ __device__ void producer_role(const typename P::Params& p, const Smem& S, const 
     }
     if (!ok && lane == 0) {
         // Let every copy still in flight land (bounded) before the CTA exits.
+        // These waits ignore the abort flag: copies complete on their own.
+        int never = 0;
+        const WaitCtx own{p.status, &never};
         const uint32_t first = issued > L.nslot ? issued - L.nslot : 0;
-        for (uint32_t j = first; j < issued; ++j) mbar_wait(bars.full(j % L.nslot), (j / L.nslot) & 1, p.status);
+        for (uint32_t j = first; j < issued; ++j) mbar_wait(bars.full(j % L.nslot), (j / L.nslot) & 1, own);
         const uint32_t sfirst = sissued > L.nss ? sissued - L.nss : 0;
-        for (uint32_t j = sfirst; j < sissued; ++j) mbar_wait(bars.sfull(j % L.nss), (j / L.nss) & 1, p.status);
+        for (uint32_t j = sfirst; j < sissued; ++j) mbar_wait(bars.sfull(j % L.nss), (j / L.nss) & 1, own);
     }
 }
 
@@ -311,42 +380,56 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
     uint8_t* xs = S.gbase + L.xs;
     float* fx = reinterpret_cast<float*>(S.gbase + L.fx);
     float* redw = reinterpret_cast<float*>(S.gbase + L.red);
-    const uint8_t* scb = S.gbase + L.sc;
+    const uint32_t xs_s = S.base + L.xs, fx_s = S.base + L.fx, scb = S.base + L.sc;
     const int nkbc = pl.kb1 - pl.kb0;
+    const bool fast_steps = (p.nblk & 7) == 0;  // 8-byte aligned scale words
     int cur_chunk = -1;
     int ncols = 0;
+    uint32_t xphase = 0;
     uint32_t i = warp;
     for (int u = pl.u0; u < pl.u1; ++u) {
         const uint32_t uu = u - pl.u0;
         const int chunk = P::chunk_of(p, u);
         if (chunk != cur_chunk) {
-            // Everyone is done with the previous columns before they change.
-            named_barrier_sync(1, kConsumerThreads);
-            P::stage(p, chunk, pl.kblk0, pl.kblk1, xs, fx, warp * 32 + lane, kConsumerThreads);
-            named_barrier_sync(1, kConsumerThreads);
+            // Everyone is done with the previous columns before they change,
+            // and the new ones are complete before anyone reads them. The
+            // barriers are mbarriers so a wait can give up instead of hang.
+            __syncwarp();
+            if (lane == 0) mbar_arrive(S.xbars);
+            if (!warp_wait(S.xbars, xphase & 1, S.wait)) return;
+            P::stage(p, chunk, pl.kblk0, pl.kblk1, xs, fx, warp * 32 + lane, Roles<P>::kConsumerThreads);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(S.xbars + 8);
+            if (!warp_wait(S.xbars + 8, xphase & 1, S.wait)) return;
+            ++xphase;
             cur_chunk = chunk;
             ncols = P::ncols(p, chunk);
         }
         const uint32_t ss = uu % L.nss;
-        if (!warp_wait(bars.sfull(ss), (uu / L.nss) & 1, p.status)) return;
-        const uint8_t* sc = scb + ss * L.ss_bytes;
+        if (!warp_wait(bars.sfull(ss), (uu / L.nss) & 1, S.wait)) return;
+        const uint32_t sc = scb + ss * L.ss_bytes;
         float acc[BOXES][NT][4];
 #pragma unroll
         for (int bx = 0; bx < BOXES; ++bx)
 #pragma unroll
             for (int n = 0; n < NT; ++n) acc[bx][n][0] = acc[bx][n][1] = acc[bx][n][2] = acc[bx][n][3] = 0.f;
         const uint32_t ib = uu * nkbc;
-        for (; i < ib + nkbc; i += kConsumerWarps) {
+        for (; i < ib + nkbc; i += P::NCW) {
             const uint32_t slot = i % L.nslot;
-            if (!warp_wait(bars.full(slot), (i / L.nslot) & 1, p.status)) return;
-            consume_step<NT, BOXES>(S.base + L.ring + slot * kSlotBytes, sc, p.nblk, pl.kb0 + static_cast<int>(i - ib),
-                                    pl.kblk0, pl.kblk1, ncols, p.xcols, xs, fx, acc, lane);
+            if (!warp_wait(bars.full(slot), (i / L.nslot) & 1, S.wait)) return;
+            const int kb = pl.kb0 + static_cast<int>(i - ib);
+            if (fast_steps && kb * 8 + 8 <= pl.kblk1)
+                consume_step_full<NT, BOXES>(S.base + L.ring + slot * kSlotBytes, sc, p.nblk, kb, pl.kblk0, ncols,
+                                             p.xcols, xs_s, fx_s, acc, lane);
+            else
+                consume_step<NT, BOXES>(S.base + L.ring + slot * kSlotBytes, sc, p.nblk, kb, pl.kblk0, pl.kblk1,
+                                        ncols, p.xcols, xs_s, fx_s, acc, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(bars.empty(slot));
         }
         const uint32_t rb = uu & 1;
-        if (!warp_wait(bars.rempty(rb), ((uu >> 1) & 1) ^ 1, p.status)) return;
-        float* R = redw + (rb * kConsumerWarps + warp) * kRedWarpFloats;
+        if (!warp_wait(bars.rempty(rb), ((uu >> 1) & 1) ^ 1, S.wait)) return;
+        float* R = redw + (rb * P::NCW + warp) * kRedWarpFloats;
         const int g = lane >> 2, tig = lane & 3;
 #pragma unroll
         for (int bx = 0; bx < BOXES; ++bx)
@@ -381,10 +464,10 @@ __device__ void reducer_role(const typename P::Params& p, const Smem& S, const P
     for (int u = pl.u0; u < pl.u1; ++u) {
         const uint32_t uu = u - pl.u0;
         const uint32_t rb = uu & 1;
-        if (!warp_wait(bars.rfull(rb), (uu >> 1) & 1, p.status)) return;
+        if (!warp_wait(bars.rfull(rb), (uu >> 1) & 1, S.wait)) return;
         const int ncols = P::ncols(p, P::chunk_of(p, u));
         // CTA-local sums over the consumer warps, fixed order.
-        const float* R = red + rb * kConsumerWarps * kRedWarpFloats;
+        const float* R = red + rb * P::NCW * kRedWarpFloats;
         float* F = fin + rb * kFin;
         for (int e = lane; e < BOXES * ncols * 16; e += 32) {
             const int bx = e / (ncols * 16);
@@ -392,7 +475,7 @@ __device__ void reducer_role(const typename P::Params& p, const Smem& S, const P
             const int col = rem >> 4, r = rem & 15;
             float s = 0.f;
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) s += R[w * kRedWarpFloats + (bx * 8 * NT + col) * kRedStride + r];
+            for (int w = 0; w < P::NCW; ++w) s += R[w * kRedWarpFloats + (bx * 8 * NT + col) * kRedStride + r];
             F[(bx * 8 * NT + col) * 16 + r] = s;
         }
         __syncwarp();
@@ -400,7 +483,7 @@ __device__ void reducer_role(const typename P::Params& p, const Smem& S, const P
         if (pl.cl > 1) {
             if (pl.rank != 0) {
                 // Send this CTA's part of K to the leader, in its rank's slot.
-                if (!__all_sync(0xffffffffu, mbar_wait_cluster(cempty0 + 8 * rb, ((uu >> 1) & 1) ^ 1, p.status)))
+                if (!__all_sync(0xffffffffu, mbar_wait_cluster(cempty0 + 8 * rb, ((uu >> 1) & 1) ^ 1, S.wait)))
                     return;
                 const uint32_t dst = map_to_rank(S.base + L.recv + ((rb * (pl.cl - 1) + pl.rank - 1) * kFin) * 4, 0);
                 for (int e = lane; e < BOXES * ncols * 16; e += 32) {
@@ -413,7 +496,7 @@ __device__ void reducer_role(const typename P::Params& p, const Smem& S, const P
                 continue;
             }
             // Leader: add the other ranks' parts in rank order.
-            if (!__all_sync(0xffffffffu, mbar_wait_cluster(cfull0 + 8 * rb, (uu >> 1) & 1, p.status))) return;
+            if (!__all_sync(0xffffffffu, mbar_wait_cluster(cfull0 + 8 * rb, (uu >> 1) & 1, S.wait))) return;
             for (int e = lane; e < BOXES * ncols * 16; e += 32) {
                 const int bx = e / (ncols * 16);
                 const int rem = e - bx * ncols * 16;
@@ -446,7 +529,7 @@ __device__ void reducer_role(const typename P::Params& p, const Smem& S, const P
 //                                int tid, int nthreads);
 //   __device__ static void epilogue(const Params&, int u, const Sums<NT>&, int lane);
 template <class P>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Roles<P>::kThreads, 1)
     stream_kernel(const __grid_constant__ CUtensorMap tmap, const typename P::Params p) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -456,6 +539,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     S.L = p.layout;
     S.bars = Bars{S.base + S.L.bars, S.L.nslot, S.L.nss};
     S.cbars = S.base + S.L.bars + 8 * (2 * S.L.nslot + 2 * S.L.nss + 4);
+    S.xbars = S.cbars + 32;
+    S.wait = WaitCtx{p.status, reinterpret_cast<volatile int*>(S.gbase + S.L.bars + 8 * (2 * S.L.nslot + 2 * S.L.nss + 10))};
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -479,14 +564,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (uint32_t s = 0; s < S.L.nss; ++s) {
             mbar_init(bars.sfull(s), 1);
-            mbar_init(bars.sempty(s), kConsumerWarps);
+            mbar_init(bars.sempty(s), P::NCW);
         }
         for (uint32_t b = 0; b < 2; ++b) {
-            mbar_init(bars.rfull(b), kConsumerWarps);
+            mbar_init(bars.rfull(b), P::NCW);
             mbar_init(bars.rempty(b), 1);
             mbar_init(S.cbars + 8 * b, pl.cl > 1 ? 32 * (pl.cl - 1) : 1);  // cfull
             mbar_init(S.cbars + 16 + 8 * b, 32);                          // cempty
+            mbar_init(S.xbars + 8 * b, P::NCW);                            // staging
         }
+        *S.wait.abort = 0;
         fence_barrier_init();
     }
     if (pl.cl > 1)
@@ -498,9 +585,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     pl.u0 = static_cast<int>((int64_t)U * group / ngroups);
     pl.u1 = static_cast<int>((int64_t)U * (group + 1) / ngroups);
 
-    if (warp == kProducerWarp)
+    if (warp == Roles<P>::kProducer)
         producer_role<P>(p, S, pl, &tmap, lane);
-    else if (warp == kReducerWarp)
+    else if (warp == Roles<P>::kReducer)
         reducer_role<P>(p, S, pl, lane);
     else
         consumer_role<P>(p, S, pl, warp, lane);
@@ -527,7 +614,7 @@ cudaError_t launch_stream_kernel(const CUtensorMap& tmap, const typename Prob::P
     const int cl = p.cl > 1 ? p.cl : 1;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(Roles<Prob>::kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     int groups = num_sms;

@@ -61,7 +61,7 @@ inline bool plan_layout(int nt, int boxes, int nblk, int nblk_all, int xcols, in
         l.recv = off;
         off += recv_bytes;
         l.bars = al(off, 8);
-        off = l.bars + 8 * (2 * nslot + 2 * nss + 4 + 4);
+        off = l.bars + 8 * (2 * nslot + 2 * nss + 4 + 4 + 2) + 8;  // + staging barriers + abort flag
         l.total = off;
         if (static_cast<int>(off) <= budget) {
             *out = l;

@@ -21,6 +21,9 @@ template <int NT_>
 struct DenseProblem {
     static constexpr int NT = NT_;
     static constexpr int BOXES = 1;
+    // More consumer warps hide more latency; fewer leave more registers for
+    // the wider token tiles.
+    static constexpr int NCW = NT == 1 ? 16 : (NT == 2 ? 12 : 8);
     using Params = LinearParams;
 
     __device__ static int num_units(const Params& p) { return p.n_rg; }
@@ -72,7 +75,9 @@ bool plan_linear(int T, int K, int max_smem, int* cl, SmemLayout* L) {
         if (c > 1 && c > nkb) break;
         const int nkb_c = (nkb + c - 1) / c;
         const int nb_local = nkb_c * 8 < nblk ? nkb_c * 8 : nblk;
-        if (plan_layout(tokens_to_nt(T), 1, nb_local, nblk, T, c, kConsumerWarps, kRedStride, max_smem, L)) {
+        const int nt = tokens_to_nt(T);
+        const int ncw = nt == 1 ? DenseProblem<1>::NCW : (nt == 2 ? DenseProblem<2>::NCW : DenseProblem<4>::NCW);
+        if (plan_layout(nt, 1, nb_local, nblk, T, c, ncw, kRedStride, max_smem, L)) {
             *cl = c;
             return true;
         }

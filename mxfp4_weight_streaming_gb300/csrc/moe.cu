@@ -246,6 +246,7 @@ struct GateUpParams {
 struct GateUpProblem {
     static constexpr int NT = 1;
     static constexpr int BOXES = 2;
+    static constexpr int NCW = 12;
     using Params = GateUpParams;
 
     __device__ static int num_units(const Params& p) { return *(volatile const int*)&p.w.header[0] * p.upc; }
@@ -314,6 +315,7 @@ struct DownParams {
 struct DownProblem {
     static constexpr int NT = 1;
     static constexpr int BOXES = 1;
+    static constexpr int NCW = 16;
     using Params = DownParams;
 
     __device__ static int num_units(const Params& p) { return *(volatile const int*)&p.w.header[1] * p.upc; }
@@ -404,7 +406,7 @@ int launch_moe(const CUtensorMap& map1, const CUtensorMap& map2, const MoeArgs& 
     g.xcols = kChunkGateUp;
     g.upc = a.inter / 16;
     g.cl = 1;
-    if (!plan_layout(1, 2, g.nblk, g.nblk, g.xcols, 1, kConsumerWarps, kRedStride, max_smem, &g.layout))
+    if (!plan_layout(1, 2, g.nblk, g.nblk, g.xcols, 1, GateUpProblem::NCW, kRedStride, max_smem, &g.layout))
         return MXFP4_ERR_SHAPE;
 
     DownParams d{};
@@ -418,7 +420,7 @@ int launch_moe(const CUtensorMap& map1, const CUtensorMap& map2, const MoeArgs& 
     d.xcols = 2 * kChunkDown;
     d.upc = a.hidden / 16;
     d.cl = 1;
-    if (!plan_layout(1, 1, d.nblk, d.nblk, d.xcols, 1, kConsumerWarps, kRedStride, max_smem, &d.layout))
+    if (!plan_layout(1, 1, d.nblk, d.nblk, d.xcols, 1, DownProblem::NCW, kRedStride, max_smem, &d.layout))
         return MXFP4_ERR_SHAPE;
 
     const int route_smem = static_cast<int>(P * 4 + 32 * 32 * 4);

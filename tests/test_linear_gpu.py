@@ -65,6 +65,21 @@ def test_linear_many_tokens(t):
     assert_within(bf16_to_f64(y), y_ref, rss, f"linear t={t}")
 
 
+@pytest.mark.parametrize("t,k,n", [(16, 7168, 130), (32, 7168, 70), (24, 14336, 40), (8, 16384, 33),
+                                   (12, 30720, 17)])
+def test_linear_cluster_split_k(t, k, n):
+    """Token counts whose staged activations exceed one SM: K is split over a
+    thread-block cluster and the partial sums meet through DSMEM."""
+    mx = lib()
+    w, x = linear_case(60 + t, t, k, n)
+    wq, ws, rq, rs = _pack_both(w)
+    y = mx.linear(x, wq, ws)
+    torch.cuda.synchronize()
+    y_ref, rss = oracle.linear(x, rq, rs)
+    assert_within(bf16_to_f64(y), y_ref, rss, f"cluster t={t} k={k} n={n}")
+    assert mx.last_device_status() == mx.MXFP4_OK
+
+
 def test_linear_config1_full():
     """T=1, K=N=1024, seed 0: whole output against the oracle."""
     mx = lib()

@@ -132,6 +132,32 @@ int mxfp4_moe(const void* x, int64_t t, int64_t hidden, const float* router_logi
               void* stream);
 
 /*
+ * Capacity in bytes of the scratch array built into the library for
+ * mxfp4_moe_noalloc (held on every GPU that loads the library).
+ */
+#define MXFP4_MOE_NOALLOC_SCRATCH_BYTES ((size_t)12 << 20)
+
+/*
+ * mxfp4_moe without a workspace argument, for callers that cannot allocate
+ * device memory where they run the layer: plugins whose host framework's
+ * memory pool owns the device memory, serving loops that forbid allocation
+ * after warm-up, and latency-bound loops that cannot take cudaMalloc's
+ * implicit synchronisation. The pages have no counterpart to this entry
+ * point.
+ *   Arguments, layouts and results are those of mxfp4_moe, minus
+ *   `workspace` / `workspace_bytes`.
+ *   Scratch: a fixed device array of MXFP4_MOE_NOALLOC_SCRATCH_BYTES (12 MiB)
+ *   inside the library. Problems needing more (mxfp4_moe_workspace_size)
+ *   return MXFP4_ERR_WORKSPACE before any launch.
+ *   The first call on a device looks up the array's device address; make
+ *   it before any stream capture. Calls share the array: calls that overlap
+ *   on the GPU race. Nothing is allocated or freed.
+ */
+int mxfp4_moe_noalloc(const void* x, int64_t t, int64_t hidden, const float* router_logits, int64_t e, int top_k,
+                      const uint8_t* w1q, const uint8_t* w1s, const uint8_t* w2q, const uint8_t* w2s, int64_t inter,
+                      void* y, int32_t* topk_ids, float* topk_w, void* stream);
+
+/*
  * Synchronizes `stream`, then returns MXFP4_OK, MXFP4_ERR_TIMEOUT if some
  * kernel of this library on the current device gave up a bounded wait since
  * the last call, or MXFP4_ERR_CUDA if the stream reports an error. Clears

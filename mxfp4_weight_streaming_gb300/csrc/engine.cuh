@@ -302,68 +302,74 @@ struct Smem {
 template <class P>
 __device__ void producer_role(const typename P::Params& p, const Smem& S, const Placement& pl,
                               const CUtensorMap* tmap, int lane) {
+    // One lane issues everything: per unit one scale copy, per stage (L.steps
+    // K steps of BOXES boxes) one expect_tx and the stage's TMA loads. A
+    // stage carries 8-16 KB, so the per-copy barrier traffic stays small.
+    if (lane != 0) return;
     constexpr int BOXES = P::BOXES;
-    constexpr uint32_t kSlotBytes = BOXES * kBoxBytes;
     const SmemLayout& L = S.L;
     const Bars& bars = S.bars;
+    const uint32_t spb = L.steps;
+    const uint32_t stage_bytes = spb * BOXES * kBoxBytes;
     const uint32_t scale_bytes = 16u * static_cast<uint32_t>(p.nblk);
+    const int nkbc = pl.kb1 - pl.kb0;
     const uint64_t policy = l2_evict_first_policy();
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
     bool ok = true;
-    uint32_t issued = 0, sissued = 0;
+    uint32_t staged = 0, sissued = 0;
     for (int u = pl.u0; u < pl.u1 && ok; ++u) {
         const uint32_t uu = u - pl.u0;
         const uint32_t ss = uu % L.nss;
-        if (lane == 0) ok = mbar_wait(bars.sempty(ss), ((uu / L.nss) & 1) ^ 1, S.wait);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
+        if (!mbar_wait(bars.sempty(ss), ((uu / L.nss) & 1) ^ 1, S.wait)) {
+            ok = false;
+            break;
+        }
+        // Scale rows of the unit: a bulk copy of the 16-byte-aligned part, and
+        // (only for a tail row group) the last few bytes stored by this lane.
         const uint32_t bytes = static_cast<uint32_t>(P::unit_rows(p, u)) * static_cast<uint32_t>(p.nblk);
+        const uint32_t bulk = bytes & ~15u;
         const uint32_t dst = S.base + L.sc + ss * L.ss_bytes;
-        if ((bytes & 15u) == 0) {
-            if (lane == 0) {
-                mbar_arrive_expect_tx(bars.sfull(ss), bytes * BOXES);
+        uint8_t* dst_g = S.gbase + L.sc + ss * L.ss_bytes;
 #pragma unroll
-                for (int bx = 0; bx < BOXES; ++bx)
-                    bulk_load(dst + bx * scale_bytes, P::scale_src(p, u, bx), bytes, bars.sfull(ss), policy);
-            }
-        } else {
-            uint8_t* d = S.gbase + L.sc + ss * L.ss_bytes;
+        for (int bx = 0; bx < BOXES; ++bx) {
+            const uint8_t* src = P::scale_src(p, u, bx);
+            for (uint32_t b = bulk; b < bytes; ++b) dst_g[bx * scale_bytes + b] = src[b];
+        }
+        mbar_arrive_expect_tx(bars.sfull(ss), bulk * BOXES);
+        if (bulk) {
 #pragma unroll
-            for (int bx = 0; bx < BOXES; ++bx) {
-                const uint8_t* src = P::scale_src(p, u, bx);
-                for (uint32_t b = lane; b < bytes; b += 32) d[bx * scale_bytes + b] = src[b];
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bars.sfull(ss));
+            for (int bx = 0; bx < BOXES; ++bx)
+                bulk_load(dst + bx * scale_bytes, P::scale_src(p, u, bx), bulk, bars.sfull(ss), policy);
         }
         ++sissued;
         int rows[BOXES];
 #pragma unroll
         for (int bx = 0; bx < BOXES; ++bx) rows[bx] = P::box_row(p, u, bx);
-        for (int kb = pl.kb0; kb < pl.kb1; ++kb) {
-            const uint32_t slot = issued % L.nslot;
-            const uint32_t ph = (issued / L.nslot) & 1;
-            if (lane == 0) {
-                ok = mbar_wait(bars.empty(slot), ph ^ 1, S.wait);
-                if (ok) {
-                    mbar_arrive_expect_tx(bars.full(slot), kSlotBytes);
-#pragma unroll
-                    for (int bx = 0; bx < BOXES; ++bx)
-                        tma_load_2d(S.base + L.ring + slot * kSlotBytes + bx * kBoxBytes, tmap, kb * 128, rows[bx],
-                                    bars.full(slot), policy);
-                }
+        for (int st = 0; st < nkbc; st += static_cast<int>(spb)) {
+            const uint32_t slot = staged % L.nslot;
+            if (!mbar_wait(bars.empty(slot), ((staged / L.nslot) & 1) ^ 1, S.wait)) {
+                ok = false;
+                break;
             }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            ++issued;
+            mbar_arrive_expect_tx(bars.full(slot), stage_bytes);
+            const uint32_t sbase = S.base + L.ring + slot * stage_bytes;
+            for (uint32_t j = 0; j < spb; ++j) {
+                const int kb = pl.kb0 + st + static_cast<int>(j);
+#pragma unroll
+                for (int bx = 0; bx < BOXES; ++bx)
+                    tma_load_2d(sbase + (j * BOXES + bx) * kBoxBytes, tmap, kb * 128, rows[bx], bars.full(slot),
+                                policy);
+            }
+            ++staged;
         }
     }
-    if (!ok && lane == 0) {
+    if (!ok) {
         // Let every copy still in flight land (bounded) before the CTA exits.
         // These waits ignore the abort flag: copies complete on their own.
         int never = 0;
         const WaitCtx own{p.status, &never};
-        const uint32_t first = issued > L.nslot ? issued - L.nslot : 0;
-        for (uint32_t j = first; j < issued; ++j) mbar_wait(bars.full(j % L.nslot), (j / L.nslot) & 1, own);
+        const uint32_t first = staged > L.nslot ? staged - L.nslot : 0;
+        for (uint32_t j = first; j < staged; ++j) mbar_wait(bars.full(j % L.nslot), (j / L.nslot) & 1, own);
         const uint32_t sfirst = sissued > L.nss ? sissued - L.nss : 0;
         for (uint32_t j = sfirst; j < sissued; ++j) mbar_wait(bars.sfull(j % L.nss), (j / L.nss) & 1, own);
     }
@@ -373,10 +379,11 @@ template <class P>
 __device__ void consumer_role(const typename P::Params& p, const Smem& S, const Placement& pl, int warp, int lane) {
     constexpr int NT = P::NT;
     constexpr int BOXES = P::BOXES;
-    constexpr uint32_t kSlotBytes = BOXES * kBoxBytes;
     constexpr int kRedWarpFloats = BOXES * 8 * NT * kRedStride;
     const SmemLayout& L = S.L;
     const Bars& bars = S.bars;
+    const uint32_t spb = L.steps;
+    const uint32_t stage_bytes = spb * BOXES * kBoxBytes;
     uint8_t* xs = S.gbase + L.xs;
     float* fx = reinterpret_cast<float*>(S.gbase + L.fx);
     float* redw = reinterpret_cast<float*>(S.gbase + L.red);
@@ -415,15 +422,19 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
             for (int n = 0; n < NT; ++n) acc[bx][n][0] = acc[bx][n][1] = acc[bx][n][2] = acc[bx][n][3] = 0.f;
         const uint32_t ib = uu * nkbc;
         for (; i < ib + nkbc; i += P::NCW) {
-            const uint32_t slot = i % L.nslot;
-            if (!warp_wait(bars.full(slot), (i / L.nslot) & 1, S.wait)) return;
+            // Steps are grouped in stages of spb (spb divides the steps of a
+            // unit, so a stage never straddles two units).
+            const uint32_t stage = i / spb;
+            const uint32_t slot = stage % L.nslot;
+            if (!warp_wait(bars.full(slot), (stage / L.nslot) & 1, S.wait)) return;
+            const uint32_t step_smem = S.base + L.ring + slot * stage_bytes + (i - stage * spb) * BOXES * kBoxBytes;
             const int kb = pl.kb0 + static_cast<int>(i - ib);
             if (fast_steps && kb * 8 + 8 <= pl.kblk1)
-                consume_step_full<NT, BOXES>(S.base + L.ring + slot * kSlotBytes, sc, p.nblk, kb, pl.kblk0, ncols,
-                                             p.xcols, xs_s, fx_s, acc, lane);
+                consume_step_full<NT, BOXES>(step_smem, sc, p.nblk, kb, pl.kblk0, ncols, p.xcols, xs_s, fx_s, acc,
+                                             lane);
             else
-                consume_step<NT, BOXES>(S.base + L.ring + slot * kSlotBytes, sc, p.nblk, kb, pl.kblk0, pl.kblk1,
-                                        ncols, p.xcols, xs_s, fx_s, acc, lane);
+                consume_step<NT, BOXES>(step_smem, sc, p.nblk, kb, pl.kblk0, pl.kblk1, ncols, p.xcols, xs_s, fx_s,
+                                        acc, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(bars.empty(slot));
         }
@@ -560,7 +571,7 @@ __global__ void __launch_bounds__(Roles<P>::kThreads, 1)
         const Bars& bars = S.bars;
         for (uint32_t s = 0; s < S.L.nslot; ++s) {
             mbar_init(bars.full(s), 1);
-            mbar_init(bars.empty(s), 1);
+            mbar_init(bars.empty(s), S.L.steps);  // one arrival per K step of the stage
         }
         for (uint32_t s = 0; s < S.L.nss; ++s) {
             mbar_init(bars.sfull(s), 1);

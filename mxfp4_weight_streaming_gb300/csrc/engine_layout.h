@@ -7,8 +7,9 @@ namespace mxfp4 {
 
 // Byte offsets inside the 1024-aligned dynamic shared memory of one CTA.
 struct SmemLayout {
-    uint32_t ring;      // weight ring: nslot slots of BOXES x 2048 bytes
+    uint32_t ring;      // weight ring: nslot stages of steps x BOXES x 2048 bytes
     uint32_t nslot;
+    uint32_t steps;     // K steps (256 values) per stage; divides every CTA's steps per unit
     uint32_t xs;        // staged activations, f16 [blocks][xcols][32]
     uint32_t fx;        // activation block factors, f32 [blocks][8*NT]
     uint32_t sc;        // scale ring: nss slots of ss_bytes
@@ -21,16 +22,24 @@ struct SmemLayout {
     uint32_t total;
 };
 
-// Picks the deepest weight ring (<= 64 slots) that fits next to the staged
-// activations; the scale ring is deep enough that the producer is never held
-// back by it. Returns false if not even a 16-slot ring fits.
+// K steps per stage: the largest count <= 8 / boxes that divides every
+// CTA's steps per unit (steps_a and steps_b; 0 counts as divisible).
+inline int stage_steps(int boxes, int steps_a, int steps_b) {
+    for (int s = 8 / boxes; s > 1; --s)
+        if (steps_a % s == 0 && steps_b % s == 0) return s;
+    return 1;
+}
+
+// Picks the deepest weight ring (<= 128 KB, >= 2 stages) that fits next to
+// the staged activations; the scale ring is deep enough that the producer is
+// never held back by it. Returns false if nothing fits.
 // nblk is the number of 32-blocks this CTA stages (its part of K); nblk_all
-// is the whole row's count (scales cover all of K).
+// is the whole row's count (scales cover all of K); steps is the stage size.
 inline bool plan_layout(int nt, int boxes, int nblk, int nblk_all, int xcols, int cl, int consumer_warps,
-                        int red_stride, int max_smem, SmemLayout* out) {
+                        int red_stride, int steps, int max_smem, SmemLayout* out) {
     auto al = [](uint32_t v, uint32_t a) { return (v + a - 1) / a * a; };
     const int nkb = (nblk + 7) / 8;
-    const uint32_t slot_bytes = 2048u * boxes;
+    const uint32_t slot_bytes = 2048u * boxes * steps;
     const uint32_t xs_bytes = al(static_cast<uint32_t>(nblk) * xcols * 64, 16);
     const uint32_t fx_bytes = al(static_cast<uint32_t>(nblk) * 8 * nt * 4, 16);
     const uint32_t ss_bytes = al(static_cast<uint32_t>(boxes) * 16 * nblk_all, 16);
@@ -38,13 +47,15 @@ inline bool plan_layout(int nt, int boxes, int nblk, int nblk_all, int xcols, in
     const uint32_t fin_bytes = 2u * boxes * 8 * nt * 16 * 4;
     const uint32_t recv_bytes = cl > 1 ? fin_bytes * (cl - 1) : 0;
     const int budget = max_smem - 1024;
-    for (int nslot = 64 / boxes; nslot >= 16 / boxes; --nslot) {
-        int nss = (nslot + nkb - 1) / nkb + 1;
+    const int max_slots = static_cast<int>((128u * 1024u) / slot_bytes) < 2 ? 2 : static_cast<int>((128u * 1024u) / slot_bytes);
+    for (int nslot = max_slots; nslot >= 2; --nslot) {
+        int nss = (nslot * steps + nkb - 1) / (nkb > 0 ? nkb : 1) + 1;
         nss = nss < 2 ? 2 : (nss > 16 ? 16 : nss);
         SmemLayout l{};
         uint32_t off = 0;
         l.ring = off;
         l.nslot = nslot;
+        l.steps = steps;
         off += nslot * slot_bytes;
         l.xs = off;
         off += xs_bytes;

@@ -77,7 +77,22 @@ bool plan_linear(int T, int K, int max_smem, int* cl, SmemLayout* L) {
         const int nb_local = nkb_c * 8 < nblk ? nkb_c * 8 : nblk;
         const int nt = tokens_to_nt(T);
         const int ncw = nt == 1 ? DenseProblem<1>::NCW : (nt == 2 ? DenseProblem<2>::NCW : DenseProblem<4>::NCW);
-        if (plan_layout(nt, 1, nb_local, nblk, T, c, ncw, kRedStride, max_smem, L)) {
+        // The stage size must divide the K steps of every rank (the same split
+        // the kernel uses: rank r takes [min(nkb, r*nkb_c), min(nkb, +nkb_c))).
+        int g = 0;  // gcd of the ranks' step counts (a rank with none adds nothing)
+        for (int r = 0; r < c; ++r) {
+            const int k0 = r * nkb_c < nkb ? r * nkb_c : nkb;
+            const int k1 = k0 + nkb_c < nkb ? k0 + nkb_c : nkb;
+            int a = g, b = k1 - k0;
+            while (b) {
+                const int t = a % b;
+                a = b;
+                b = t;
+            }
+            g = a;
+        }
+        const int steps = stage_steps(1, g, 0);
+        if (plan_layout(nt, 1, nb_local, nblk, T, c, ncw, kRedStride, steps, max_smem, L)) {
             *cl = c;
             return true;
         }

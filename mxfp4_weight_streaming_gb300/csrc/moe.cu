@@ -406,7 +406,8 @@ int launch_moe(const CUtensorMap& map1, const CUtensorMap& map2, const MoeArgs& 
     g.xcols = kChunkGateUp;
     g.upc = a.inter / 16;
     g.cl = 1;
-    if (!plan_layout(1, 2, g.nblk, g.nblk, g.xcols, 1, GateUpProblem::NCW, kRedStride, max_smem, &g.layout))
+    if (!plan_layout(1, 2, g.nblk, g.nblk, g.xcols, 1, GateUpProblem::NCW, kRedStride, stage_steps(2, g.nkb, 0),
+                     max_smem, &g.layout))
         return MXFP4_ERR_SHAPE;
 
     DownParams d{};
@@ -420,7 +421,8 @@ int launch_moe(const CUtensorMap& map1, const CUtensorMap& map2, const MoeArgs& 
     d.xcols = 2 * kChunkDown;
     d.upc = a.hidden / 16;
     d.cl = 1;
-    if (!plan_layout(1, 1, d.nblk, d.nblk, d.xcols, 1, DownProblem::NCW, kRedStride, max_smem, &d.layout))
+    if (!plan_layout(1, 1, d.nblk, d.nblk, d.xcols, 1, DownProblem::NCW, kRedStride, stage_steps(1, d.nkb, 0),
+                     max_smem, &d.layout))
         return MXFP4_ERR_SHAPE;
 
     const int route_smem = static_cast<int>(P * 4 + 32 * 32 * 4);

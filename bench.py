@@ -34,7 +34,9 @@ sys.path.insert(0, ROOT)
 
 METRIC = "effective HBM GB/s (% of GB300 peak) and us/call, MXFP4 GEMM at T=1-32"
 FALLBACK_HBM_GBS = 6800.0  # fallback peak when no measured peak file is present
-KERNEL_SOURCES = ["mxfp4_weight_streaming_gb300/csrc/linear.cu", "mxfp4_weight_streaming_gb300/csrc/device_common.cuh"]
+KERNEL_SOURCES = ["mxfp4_weight_streaming_gb300/csrc/linear.cu", "mxfp4_weight_streaming_gb300/csrc/engine.cuh",
+                  "mxfp4_weight_streaming_gb300/csrc/engine_layout.h",
+                  "mxfp4_weight_streaming_gb300/csrc/device_common.cuh"]
 
 WORKLOADS = {
     "linear_t1_k1024_n1024": dict(t=1, k=1024, n=1024, seed=0, x64=False),
@@ -323,7 +325,7 @@ def run_ours(args, wl_name: str, rank: int, world: int, device, with_cpu_baselin
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": profiled_traffic(wl_name),
                      "peak_source": f"{peak_src} (HBM copy bandwidth)",
-                     "kernel": "mxfp4::linear_kernel", "avg_launch_us": round(avg_launch_ms * 1e3, 4),
+                     "kernel": "mxfp4::stream_kernel<DenseProblem>", "avg_launch_us": round(avg_launch_ms * 1e3, 4),
                      "algorithmic_bytes_per_launch": bytes_call},
         "clocks": clocks.summary(wall0 - 1.5, wall1 + 0.1),
     }

@@ -61,20 +61,45 @@ int device_info(DeviceInfo** out) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Packed weights viewed as a 2D uint8 tensor [rows, k/2], boxes of
-// 16 rows x 128 bytes with the 128-byte swizzle.
-int encode_weight_map(CUtensorMap* map, const uint8_t* wq, int64_t rows, int64_t k) {
+// Packed weights [rows, k/2] as a TMA tensor map with the 128-byte swizzle.
+// With k % 256 == 0 the map is the 3D view (128 B, rows, k/256 segments of
+// 128 B): one copy lands `steps` segments of 16 rows as [step][row][128 B].
+// Otherwise it is the 2D view (k/2 B, rows) fetched one 16 x 128-byte box at
+// a time (the 3D view would let the last segment of the last row run past
+// the end of the array). Returns whether the 3D view was used in *is3d.
+int encode_weight_map(CUtensorMap* map, const uint8_t* wq, int64_t rows, int64_t k, int steps, int* is3d) {
+    CUresult r;
+    if (k % 256 == 0) {
+        cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(k / 256)};
+        cuuint64_t strides[2] = {static_cast<cuuint64_t>(k / 2), 128};
+        cuuint32_t box[3] = {128, 16, static_cast<cuuint32_t>(steps)};
+        cuuint32_t estride[3] = {1, 1, 1};
+        r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(wq), dims, strides, box, estride,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r == CUDA_SUCCESS) {
+            *is3d = 1;
+            return MXFP4_OK;
+        }
+    }
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(k / 2), static_cast<cuuint64_t>(rows)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(k / 2)};
     cuuint32_t box[2] = {128, 16};
     cuuint32_t estride[2] = {1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(wq), dims, strides, box,
-                          estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(wq), dims, strides, box, estride,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    *is3d = 0;
     return r == CUDA_SUCCESS ? MXFP4_OK : MXFP4_ERR_CUDA;
 }
 
 }  // namespace
+
+namespace mxfp4 {
+int encode_weights(CUtensorMap* map, const uint8_t* wq, int64_t rows, int64_t k, int steps, int* is3d) {
+    return encode_weight_map(map, wq, rows, k, steps, is3d);
+}
+}  // namespace mxfp4
 
 extern "C" {
 
@@ -112,7 +137,7 @@ int mxfp4_linear(const void* x, int64_t t, int64_t k, const uint8_t* wq, const u
     if (!mxfp4::plan_linear(static_cast<int>(t), static_cast<int>(k), d->max_smem, &p.cl, &p.layout))
         return MXFP4_ERR_SHAPE;
     CUtensorMap map;
-    if (int rc = encode_weight_map(&map, wq, n, k)) return rc;
+    if (int rc = encode_weight_map(&map, wq, n, k, static_cast<int>(p.layout.steps), &p.tma3d)) return rc;
     p.x = static_cast<const __nv_bfloat16*>(x);
     p.ws = ws;
     p.y = static_cast<__nv_bfloat16*>(y);
@@ -168,10 +193,7 @@ int mxfp4_moe(const void* x, int64_t t, int64_t hidden, const float* router_logi
     a.top_k = top_k;
     a.hidden = static_cast<int>(hidden);
     a.inter = static_cast<int>(inter);
-    CUtensorMap map1, map2;
-    if (int rc = encode_weight_map(&map1, w1q, e * 2 * inter, hidden)) return rc;
-    if (int rc = encode_weight_map(&map2, w2q, e * hidden, inter)) return rc;
-    return mxfp4::launch_moe(map1, map2, a, d->num_sms, d->max_smem, static_cast<cudaStream_t>(stream));
+    return mxfp4::launch_moe(w1q, w2q, a, d->num_sms, d->max_smem, static_cast<cudaStream_t>(stream));
 }
 
 int mxfp4_last_device_status(void* stream) {

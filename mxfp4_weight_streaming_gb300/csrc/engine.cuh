@@ -152,8 +152,8 @@ __device__ __forceinline__ void stage_f32_block_split(const float (&v)[32], uint
 // fewer at the end of K), against the staged columns. Blocks are numbered
 // globally (scales) and relative to kblk0 (staged activations).
 template <int NT, int BOXES>
-__device__ __forceinline__ void consume_step(uint32_t slot, uint32_t sc, int nblk, int kb, int kblk0, int kblk1,
-                                             int ncols, int xcols, uint32_t xs, uint32_t fx,
+__device__ __forceinline__ void consume_step(uint32_t slot, uint32_t box_stride, uint32_t sc, int nblk, int kb,
+                                             int kblk0, int kblk1, int ncols, int xcols, uint32_t xs, uint32_t fx,
                                              float (&acc)[BOXES][NT][4], int lane) {
     const int g = lane >> 2;
     const int tig = lane & 3;
@@ -169,7 +169,7 @@ __device__ __forceinline__ void consume_step(uint32_t slot, uint32_t sc, int nbl
         uint32_t r[BOXES][4];
 #pragma unroll
         for (int bx = 0; bx < BOXES; ++bx)
-            ldmatrix_x4(slot + bx * kBoxBytes + roff, r[bx][0], r[bx][1], r[bx][2], r[bx][3]);
+            ldmatrix_x4(slot + bx * box_stride + roff, r[bx][0], r[bx][1], r[bx][2], r[bx][3]);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             const int b = b_first + h;
@@ -212,9 +212,9 @@ __device__ __forceinline__ void consume_step(uint32_t slot, uint32_t sc, int nbl
 // scale bytes of 8 blocks read as one 8-byte word per row (needs K % 256
 // == 0 so the words are aligned).
 template <int NT, int BOXES>
-__device__ __forceinline__ void consume_step_full(uint32_t slot, uint32_t sc, int nblk, int kb, int kblk0, int ncols,
-                                                  int xcols, uint32_t xs, uint32_t fx, float (&acc)[BOXES][NT][4],
-                                                  int lane) {
+__device__ __forceinline__ void consume_step_full(uint32_t slot, uint32_t box_stride, uint32_t sc, int nblk, int kb,
+                                                  int kblk0, int ncols, int xcols, uint32_t xs, uint32_t fx,
+                                                  float (&acc)[BOXES][NT][4], int lane) {
     const int g = lane >> 2;
     const int tig = lane & 3;
     const int mi = lane >> 3;
@@ -226,7 +226,7 @@ __device__ __forceinline__ void consume_step_full(uint32_t slot, uint32_t sc, in
     for (int bx = 0; bx < BOXES; ++bx)
 #pragma unroll
         for (int jp = 0; jp < 4; ++jp)
-            ldmatrix_x4(slot + bx * kBoxBytes + row * 128 + (((2 * jp + bsel) ^ (row & 7)) << 4), r[bx][jp][0],
+            ldmatrix_x4(slot + bx * box_stride + row * 128 + (((2 * jp + bsel) ^ (row & 7)) << 4), r[bx][jp][0],
                         r[bx][jp][1], r[bx][jp][2], r[bx][jp][3]);
     uint2 s0[BOXES], s1[BOXES];
 #pragma unroll
@@ -352,13 +352,22 @@ __device__ void producer_role(const typename P::Params& p, const Smem& S, const 
                 break;
             }
             mbar_arrive_expect_tx(bars.full(slot), stage_bytes);
+            // Stage layout: [box][step][16 rows][128 B], 128-byte swizzle.
             const uint32_t sbase = S.base + L.ring + slot * stage_bytes;
-            for (uint32_t j = 0; j < spb; ++j) {
-                const int kb = pl.kb0 + st + static_cast<int>(j);
+            if (p.tma3d) {
+                // One copy per box: 16 rows x spb 128-byte segments of K.
 #pragma unroll
                 for (int bx = 0; bx < BOXES; ++bx)
-                    tma_load_2d(sbase + (j * BOXES + bx) * kBoxBytes, tmap, kb * 128, rows[bx], bars.full(slot),
+                    tma_load_3d(sbase + bx * spb * kBoxBytes, tmap, 0, rows[bx], pl.kb0 + st, bars.full(slot),
                                 policy);
+            } else {
+                for (uint32_t j = 0; j < spb; ++j) {
+                    const int kb = pl.kb0 + st + static_cast<int>(j);
+#pragma unroll
+                    for (int bx = 0; bx < BOXES; ++bx)
+                        tma_load_2d(sbase + (bx * spb + j) * kBoxBytes, tmap, kb * 128, rows[bx], bars.full(slot),
+                                    policy);
+                }
             }
             ++staged;
         }
@@ -427,14 +436,15 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
             const uint32_t stage = i / spb;
             const uint32_t slot = stage % L.nslot;
             if (!warp_wait(bars.full(slot), (stage / L.nslot) & 1, S.wait)) return;
-            const uint32_t step_smem = S.base + L.ring + slot * stage_bytes + (i - stage * spb) * BOXES * kBoxBytes;
+            const uint32_t box_stride = spb * kBoxBytes;
+            const uint32_t step_smem = S.base + L.ring + slot * stage_bytes + (i - stage * spb) * kBoxBytes;
             const int kb = pl.kb0 + static_cast<int>(i - ib);
             if (fast_steps && kb * 8 + 8 <= pl.kblk1)
-                consume_step_full<NT, BOXES>(step_smem, sc, p.nblk, kb, pl.kblk0, ncols, p.xcols, xs_s, fx_s, acc,
-                                             lane);
+                consume_step_full<NT, BOXES>(step_smem, box_stride, sc, p.nblk, kb, pl.kblk0, ncols, p.xcols, xs_s,
+                                             fx_s, acc, lane);
             else
-                consume_step<NT, BOXES>(step_smem, sc, p.nblk, kb, pl.kblk0, pl.kblk1, ncols, p.xcols, xs_s, fx_s,
-                                        acc, lane);
+                consume_step<NT, BOXES>(step_smem, box_stride, sc, p.nblk, kb, pl.kblk0, pl.kblk1, ncols, p.xcols,
+                                        xs_s, fx_s, acc, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(bars.empty(slot));
         }
@@ -527,7 +537,9 @@ __device__ void reducer_role(const typename P::Params& p, const Smem& S, const P
 // ------------------------------------------------------------------------
 // The kernel. P (the problem) supplies:
 //   static constexpr int NT, BOXES;
-//   struct Params { ...; unsigned* status; int nblk; int nkb; int xcols; int cl; SmemLayout layout; };
+//   struct Params { ...; unsigned* status; int nblk; int nkb; int xcols; int cl; int tma3d; SmemLayout layout; };
+//     tma3d = the tensor map is the 3D view (128 B, rows, K/256 segments) and one
+//     copy fetches a whole stage of a box; else it is the 2D view (K/2 B, rows).
 //     xcols = staged columns per block: xs[block][xcols][32] f16, fx[block][8*NT] f32
 //     (zero factors for unused columns); cl = CTAs per cluster splitting K.
 //   __device__ static int  num_units(const Params&);

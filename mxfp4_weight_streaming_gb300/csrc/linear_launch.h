@@ -20,6 +20,7 @@ struct LinearParams {
     int nkb;                 // ceil(K / 256): weight boxes per row group
     int xcols;               // staged columns per block (= T)
     int cl;                  // CTAs per cluster splitting K (1 = no cluster)
+    int tma3d;               // tensor map is the 3D (128 B, rows, K/256) view
     int n_rg;                // ceil(N / 16): row groups
     SmemLayout layout;
 };

@@ -238,7 +238,7 @@ struct GateUpParams {
     MoeWork w;
     unsigned* status;
     int top_k, hidden, inter;
-    int nblk, nkb, xcols, cl;
+    int nblk, nkb, xcols, cl, tma3d;
     int upc;                 // units per chunk = inter / 16
     SmemLayout layout;
 };
@@ -307,7 +307,7 @@ struct DownParams {
     MoeWork w;
     unsigned* status;
     int hidden, inter;
-    int nblk, nkb, xcols, cl;
+    int nblk, nkb, xcols, cl, tma3d;
     int upc;             // units per chunk = hidden / 16
     SmemLayout layout;
 };
@@ -388,7 +388,7 @@ __global__ void moe_combine_kernel(MoeWork w, int T, int top_k, int hidden, __nv
 }
 
 // ------------------------------------------------------------------- host
-int launch_moe(const CUtensorMap& map1, const CUtensorMap& map2, const MoeArgs& a, int num_sms, int max_smem,
+int launch_moe(const uint8_t* w1q, const uint8_t* w2q, const MoeArgs& a, int num_sms, int max_smem,
                cudaStream_t stream) {
     const int64_t P = (int64_t)a.T * a.top_k;
     MoeWork w = carve(a.workspace, P, a.hidden, a.inter, nullptr);
@@ -424,6 +424,14 @@ int launch_moe(const CUtensorMap& map1, const CUtensorMap& map2, const MoeArgs& 
     if (!plan_layout(1, 1, d.nblk, d.nblk, d.xcols, 1, DownProblem::NCW, kRedStride, stage_steps(1, d.nkb, 0),
                      max_smem, &d.layout))
         return MXFP4_ERR_SHAPE;
+
+    CUtensorMap map1, map2;
+    if (int rc = encode_weights(&map1, w1q, (int64_t)a.E * 2 * a.inter, a.hidden, static_cast<int>(g.layout.steps),
+                                &g.tma3d))
+        return rc;
+    if (int rc = encode_weights(&map2, w2q, (int64_t)a.E * a.hidden, a.inter, static_cast<int>(d.layout.steps),
+                                &d.tma3d))
+        return rc;
 
     const int route_smem = static_cast<int>(P * 4 + 32 * 32 * 4);
     if (route_smem > 48 * 1024) {

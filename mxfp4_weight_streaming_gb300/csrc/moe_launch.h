@@ -22,7 +22,10 @@ struct MoeArgs {
 };
 
 size_t moe_workspace_bytes(int64_t t, int64_t e, int top_k, int64_t hidden, int64_t inter);
-int launch_moe(const CUtensorMap& map1, const CUtensorMap& map2, const MoeArgs& a, int num_sms, int max_smem,
+int launch_moe(const uint8_t* w1q, const uint8_t* w2q, const MoeArgs& a, int num_sms, int max_smem,
                cudaStream_t stream);
+
+// Tensor map of packed weights [rows, k/2] (defined with the C ABI).
+int encode_weights(CUtensorMap* map, const uint8_t* wq, int64_t rows, int64_t k, int steps, int* is3d);
 
 }  // namespace mxfp4

@@ -44,12 +44,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// Nanoseconds a waiting thread may be suspended inside one try_wait (it is
+// woken when the phase completes); keeps idle warps from spinning on issue
+// slots the working warps need.
+constexpr uint32_t kSuspendHintNs = 20000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "n"(kSuspendHintNs)
         : "memory");
     return ok != 0;
 }
@@ -83,6 +89,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
             return false;
         }
     }
+}
+
+// ------------------------------------------- programmatic dependent launch
+// Lets the next kernel of the stream be scheduled before this one ends (its
+// CTAs become resident as SMs free up).
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the previous kernel of the stream has completed and its
+// writes are visible (a no-op when this kernel was not launched early).
+__device__ __forceinline__ void pdl_wait_previous() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // ------------------------------------------------------------ clusters

@@ -71,6 +71,20 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
 // and a bf16 value (8 significant bits) is exact in f16 when the result is
 // at least 2^-17, i.e. for every element within 2^31 of its block maximum.
 
+// Where a problem's stage() writes: column c of 32-block b (relative to the
+// CTA's first block) and its factor. Columns are 16 bytes apart in bank
+// terms (stride = blocks*64 + 16) so the 8 columns a warp reads per block
+// hit different banks; factors sit in column pairs [pair][block][2].
+struct StageDst {
+    uint8_t* xs;
+    uint8_t* fx;
+    uint32_t xs_stride, fx_stride;
+    __device__ uint8_t* col(int c, int b) const { return xs + c * xs_stride + b * 64; }
+    __device__ float* factor(int c, int b) const {
+        return reinterpret_cast<float*>(fx + (c >> 1) * fx_stride + b * 8 + (c & 1) * 4);
+    }
+};
+
 // Floor of log2 of a positive float given its bit pattern (no sign).
 __device__ __forceinline__ int floor_log2_f32_bits(uint32_t a) {
     const int e = static_cast<int>(a >> 23);
@@ -153,8 +167,8 @@ __device__ __forceinline__ void stage_f32_block_split(const float (&v)[32], uint
 // globally (scales) and relative to kblk0 (staged activations).
 template <int NT, int BOXES>
 __device__ __forceinline__ void consume_step(uint32_t slot, uint32_t box_stride, uint32_t sc, int nblk, int kb,
-                                             int kblk0, int kblk1, int ncols, int xcols, uint32_t xs, uint32_t fx,
-                                             float (&acc)[BOXES][NT][4], int lane) {
+                                             int kblk0, int kblk1, int ncols, uint32_t xs, uint32_t xs_stride,
+                                             uint32_t fx, uint32_t fx_stride, float (&acc)[BOXES][NT][4], int lane) {
     const int g = lane >> 2;
     const int tig = lane & 3;
     const int mi = lane >> 3;
@@ -181,8 +195,8 @@ __device__ __forceinline__ void consume_step(uint32_t slot, uint32_t box_stride,
             for (int n = 0; n < NT; ++n) {
                 const int col = g + 8 * n;
                 xv[n] = make_uint4(0, 0, 0, 0);
-                if (col < ncols) xv[n] = lds128(xs + (bl * xcols + col) * 64 + tig * 16);
-                f[n] = lds64f(fx + (bl * 8 * NT + 8 * n + 2 * tig) * 4);
+                if (col < ncols) xv[n] = lds128(xs + col * xs_stride + bl * 64 + tig * 16);
+                f[n] = lds64f(fx + (tig + 4 * n) * fx_stride + bl * 8);
             }
 #pragma unroll
             for (int bx = 0; bx < BOXES; ++bx) {
@@ -213,8 +227,8 @@ __device__ __forceinline__ void consume_step(uint32_t slot, uint32_t box_stride,
 // == 0 so the words are aligned).
 template <int NT, int BOXES>
 __device__ __forceinline__ void consume_step_full(uint32_t slot, uint32_t box_stride, uint32_t sc, int nblk, int kb,
-                                                  int kblk0, int ncols, int xcols, uint32_t xs, uint32_t fx,
-                                                  float (&acc)[BOXES][NT][4], int lane) {
+                                                  int kblk0, int ncols, uint32_t xs, uint32_t xs_stride, uint32_t fx,
+                                                  uint32_t fx_stride, float (&acc)[BOXES][NT][4], int lane) {
     const int g = lane >> 2;
     const int tig = lane & 3;
     const int mi = lane >> 3;
@@ -236,17 +250,24 @@ __device__ __forceinline__ void consume_step_full(uint32_t slot, uint32_t box_st
         s1[bx] = lds64(scb + (g + 8) * nblk);
     }
     const int bl0 = kb * 8 - kblk0;
+    // Per-lane bases of this step; the 8 blocks are immediate offsets.
+    uint32_t xb[NT], fb[NT];
+    bool has[NT];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+        xb[n] = xs + (g + 8 * n) * xs_stride + bl0 * 64 + tig * 16;
+        fb[n] = fx + (tig + 4 * n) * fx_stride + bl0 * 8;
+        has[n] = g + 8 * n < ncols;
+    }
 #pragma unroll
     for (int blk = 0; blk < 8; ++blk) {
-        const int bl = bl0 + blk;
         uint4 xv[NT];
         float2 f[NT];
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-            const int col = g + 8 * n;
             xv[n] = make_uint4(0, 0, 0, 0);
-            if (col < ncols) xv[n] = lds128(xs + (bl * xcols + col) * 64 + tig * 16);
-            f[n] = lds64f(fx + (bl * 8 * NT + 8 * n + 2 * tig) * 4);
+            if (has[n]) xv[n] = lds128(xb[n] + blk * 64);
+            f[n] = lds64f(fb[n] + blk * 8);
         }
         const int jp = blk >> 1, h = blk & 1;
 #pragma unroll
@@ -406,6 +427,7 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
     for (int u = pl.u0; u < pl.u1; ++u) {
         const uint32_t uu = u - pl.u0;
         const int chunk = P::chunk_of(p, u);
+        if (cur_chunk < 0) pdl_wait_previous();  // activations may come from the previous kernel
         if (chunk != cur_chunk) {
             // Everyone is done with the previous columns before they change,
             // and the new ones are complete before anyone reads them. The
@@ -413,7 +435,8 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
             __syncwarp();
             if (lane == 0) mbar_arrive(S.xbars);
             if (!warp_wait(S.xbars, xphase & 1, S.wait)) return;
-            P::stage(p, chunk, pl.kblk0, pl.kblk1, xs, fx, warp * 32 + lane, Roles<P>::kConsumerThreads);
+            P::stage(p, chunk, pl.kblk0, pl.kblk1, StageDst{xs, reinterpret_cast<uint8_t*>(fx), L.xs_stride, L.fx_stride},
+                     warp * 32 + lane, Roles<P>::kConsumerThreads);
             __syncwarp();
             if (lane == 0) mbar_arrive(S.xbars + 8);
             if (!warp_wait(S.xbars + 8, xphase & 1, S.wait)) return;
@@ -440,11 +463,11 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
             const uint32_t step_smem = S.base + L.ring + slot * stage_bytes + (i - stage * spb) * kBoxBytes;
             const int kb = pl.kb0 + static_cast<int>(i - ib);
             if (fast_steps && kb * 8 + 8 <= pl.kblk1)
-                consume_step_full<NT, BOXES>(step_smem, box_stride, sc, p.nblk, kb, pl.kblk0, ncols, p.xcols, xs_s,
-                                             fx_s, acc, lane);
+                consume_step_full<NT, BOXES>(step_smem, box_stride, sc, p.nblk, kb, pl.kblk0, ncols, xs_s,
+                                             L.xs_stride, fx_s, L.fx_stride, acc, lane);
             else
-                consume_step<NT, BOXES>(step_smem, box_stride, sc, p.nblk, kb, pl.kblk0, pl.kblk1, ncols, p.xcols,
-                                        xs_s, fx_s, acc, lane);
+                consume_step<NT, BOXES>(step_smem, box_stride, sc, p.nblk, kb, pl.kblk0, pl.kblk1, ncols, xs_s,
+                                        L.xs_stride, fx_s, L.fx_stride, acc, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(bars.empty(slot));
         }
@@ -482,6 +505,7 @@ __device__ void reducer_role(const typename P::Params& p, const Smem& S, const P
     float* fin = reinterpret_cast<float*>(S.gbase + L.fin);
     const float* recv = reinterpret_cast<const float*>(S.gbase + L.recv);
     const uint32_t cfull0 = S.cbars, cempty0 = S.cbars + 16;
+    pdl_wait_previous();  // outputs may be read or written by the previous kernel
     for (int u = pl.u0; u < pl.u1; ++u) {
         const uint32_t uu = u - pl.u0;
         const uint32_t rb = uu & 1;
@@ -538,17 +562,18 @@ __device__ void reducer_role(const typename P::Params& p, const Smem& S, const P
 // The kernel. P (the problem) supplies:
 //   static constexpr int NT, BOXES;
 //   struct Params { ...; unsigned* status; int nblk; int nkb; int xcols; int cl; int tma3d; SmemLayout layout; };
+//     xcols = staged columns (the layout's column count)
 //     tma3d = the tensor map is the 3D view (128 B, rows, K/256 segments) and one
 //     copy fetches a whole stage of a box; else it is the 2D view (K/2 B, rows).
-//     xcols = staged columns per block: xs[block][xcols][32] f16, fx[block][8*NT] f32
-//     (zero factors for unused columns); cl = CTAs per cluster splitting K.
+//     (stage() writes through StageDst and zeroes the factors of unused columns);
+//     cl = CTAs per cluster splitting K.
 //   __device__ static int  num_units(const Params&);
 //   __device__ static int  chunk_of(const Params&, int u);
 //   __device__ static int  box_row(const Params&, int u, int box);      // TMA row coordinate
 //   __device__ static const uint8_t* scale_src(const Params&, int u, int box);
 //   __device__ static int  unit_rows(const Params&, int u);            // valid rows (<= 16)
 //   __device__ static int  ncols(const Params&, int chunk);            // staged columns
-//   __device__ static void stage(const Params&, int chunk, int kblk0, int kblk1, uint8_t* xs, float* fx,
+//   __device__ static void stage(const Params&, int chunk, int kblk0, int kblk1, const StageDst&,
 //                                int tid, int nthreads);
 //   __device__ static void epilogue(const Params&, int u, const Sums<NT>&, int lane);
 template <class P>
@@ -567,6 +592,9 @@ __global__ void __launch_bounds__(Roles<P>::kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    // The next kernel on the stream may be scheduled now: it only streams
+    // weights until it has waited for this kernel (pdl_wait_previous).
+    pdl_launch_dependents();
 
     Placement pl;
     pl.cl = p.cl > 1 ? static_cast<uint32_t>(p.cl) : 1u;
@@ -636,18 +664,23 @@ cudaError_t launch_stream_kernel(const CUtensorMap& tmap, const typename Prob::P
     }
     const int cl = p.cl > 1 ? p.cl : 1;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cfg.blockDim = dim3(Roles<Prob>::kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
+    // Programmatic dependent launch: this kernel may start (and stream
+    // weights) while the previous kernel of the stream finishes.
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     int groups = num_sms;
     if (cl > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = cl;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = cl;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
         cfg.gridDim = dim3(cl * (num_sms / cl));
         int nclusters = (dev >= 0 && dev < 64 && cl <= 8) ? clusters_cached[dev][cl] : 0;
         if (nclusters == 0) {

@@ -10,8 +10,10 @@ struct SmemLayout {
     uint32_t ring;      // weight ring: nslot stages of steps x BOXES x 2048 bytes
     uint32_t nslot;
     uint32_t steps;     // K steps (256 values) per stage; divides every CTA's steps per unit
-    uint32_t xs;        // staged activations, f16 [blocks][xcols][32]
-    uint32_t fx;        // activation block factors, f32 [blocks][8*NT]
+    uint32_t xs;        // staged activations, f16 [xcols][blocks][32], column stride xs_stride
+    uint32_t fx;        // activation block factors, f32 [4*NT column pairs][blocks][2], stride fx_stride
+    uint32_t xs_stride; // bytes per staged column (blocks*64 + 16: the pad spreads columns over banks)
+    uint32_t fx_stride; // bytes per column pair of factors (blocks*8 + 16)
     uint32_t sc;        // scale ring: nss slots of ss_bytes
     uint32_t nss;
     uint32_t ss_bytes;  // one unit's scales: BOXES x 16 x K/32 bytes
@@ -40,8 +42,10 @@ inline bool plan_layout(int nt, int boxes, int nblk, int nblk_all, int xcols, in
     auto al = [](uint32_t v, uint32_t a) { return (v + a - 1) / a * a; };
     const int nkb = (nblk + 7) / 8;
     const uint32_t slot_bytes = 2048u * boxes * steps;
-    const uint32_t xs_bytes = al(static_cast<uint32_t>(nblk) * xcols * 64, 16);
-    const uint32_t fx_bytes = al(static_cast<uint32_t>(nblk) * 8 * nt * 4, 16);
+    const uint32_t xs_stride = static_cast<uint32_t>(nblk) * 64 + 16;
+    const uint32_t fx_stride = static_cast<uint32_t>(nblk) * 8 + 16;
+    const uint32_t xs_bytes = static_cast<uint32_t>(xcols) * xs_stride;
+    const uint32_t fx_bytes = static_cast<uint32_t>(4 * nt) * fx_stride;
     const uint32_t ss_bytes = al(static_cast<uint32_t>(boxes) * 16 * nblk_all, 16);
     const uint32_t red_bytes = 2u * consumer_warps * boxes * 8 * nt * red_stride * 4;
     const uint32_t fin_bytes = 2u * boxes * 8 * nt * 16 * 4;
@@ -58,8 +62,10 @@ inline bool plan_layout(int nt, int boxes, int nblk, int nblk_all, int xcols, in
         l.steps = steps;
         off += nslot * slot_bytes;
         l.xs = off;
+        l.xs_stride = xs_stride;
         off += xs_bytes;
         l.fx = off;
+        l.fx_stride = fx_stride;
         off += fx_bytes;
         l.sc = off;
         l.nss = nss;

@@ -35,7 +35,7 @@ struct DenseProblem {
     __device__ static int unit_rows(const Params& p, int u) { return min(16, p.N - u * 16); }
     __device__ static int ncols(const Params& p, int) { return p.T; }
 
-    __device__ static void stage(const Params& p, int, int kblk0, int kblk1, uint8_t* xs, float* fx, int tid,
+    __device__ static void stage(const Params& p, int, int kblk0, int kblk1, const StageDst& dst, int tid,
                                  int nthreads) {
         const int T = p.T;
         const int nb = kblk1 - kblk0;
@@ -49,10 +49,13 @@ struct DenseProblem {
             for (int q = 0; q < 4; ++q) v[q] = __ldg(src + q);
             const uint32_t w[16] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w,
                                     v[2].x, v[2].y, v[2].z, v[2].w, v[3].x, v[3].y, v[3].z, v[3].w};
-            stage_bf16_block(w, xs + (size_t)(b * p.xcols + t) * 64, fx + b * 8 * NT + t);
+            stage_bf16_block(w, dst.col(t, b), dst.factor(t, b));
         }
-        for (int it = tid; it < nb * 8 * NT; it += nthreads)
-            if (it % (8 * NT) >= T) fx[it] = 0.0f;
+        // Factors of the unused columns of the 8*NT-wide tiles are zero.
+        for (int it = tid; it < nb * (8 * NT - T); it += nthreads) {
+            const int b = it / (8 * NT - T);
+            *dst.factor(T + (it - b * (8 * NT - T)), b) = 0.0f;
+        }
     }
 
     __device__ static void epilogue(const Params& p, int u, const Sums<NT>& v, int lane) {

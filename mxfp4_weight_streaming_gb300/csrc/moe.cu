@@ -262,7 +262,7 @@ struct GateUpProblem {
     __device__ static int unit_rows(const Params&, int) { return 16; }
     __device__ static int ncols(const Params& p, int q) { return p.w.c1_cnt[q]; }
 
-    __device__ static void stage(const Params& p, int q, int kblk0, int kblk1, uint8_t* xs, float* fx, int tid,
+    __device__ static void stage(const Params& p, int q, int kblk0, int kblk1, const StageDst& dst, int tid,
                                  int nthreads) {
         const int cnt = p.w.c1_cnt[q];
         const int start = p.w.c1_start[q];
@@ -279,10 +279,12 @@ struct GateUpProblem {
             for (int k = 0; k < 4; ++k) v[k] = __ldg(src + k);
             const uint32_t wv[16] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w,
                                      v[2].x, v[2].y, v[2].z, v[2].w, v[3].x, v[3].y, v[3].z, v[3].w};
-            stage_bf16_block(wv, xs + (size_t)(b * p.xcols + t) * 64, fx + b * 8 + t);
+            stage_bf16_block(wv, dst.col(t, b), dst.factor(t, b));
         }
-        for (int it = tid; it < nb * 8; it += nthreads)
-            if ((it & 7) >= cnt) fx[it] = 0.0f;
+        for (int it = tid; it < nb * (8 - cnt); it += nthreads) {
+            const int b = it / (8 - cnt);
+            *dst.factor(cnt + (it - b * (8 - cnt)), b) = 0.0f;
+        }
     }
 
     __device__ static void epilogue(const Params& p, int u, const Sums<1>& v, int lane) {
@@ -332,7 +334,7 @@ struct DownProblem {
     __device__ static int ncols(const Params& p, int q) { return 2 * p.w.c2_cnt[q]; }
 
     // Column t holds hi(h_t), column cnt + t holds lo(h_t).
-    __device__ static void stage(const Params& p, int q, int kblk0, int kblk1, uint8_t* xs, float* fx, int tid,
+    __device__ static void stage(const Params& p, int q, int kblk0, int kblk1, const StageDst& dst, int tid,
                                  int nthreads) {
         const int cnt = p.w.c2_cnt[q];
         const int start = p.w.c2_start[q];
@@ -352,11 +354,12 @@ struct DownProblem {
                 v[4 * k + 2] = f.z;
                 v[4 * k + 3] = f.w;
             }
-            stage_f32_block_split(v, xs + (size_t)(b * p.xcols + t) * 64, xs + (size_t)(b * p.xcols + cnt + t) * 64,
-                                  fx + b * 8 + t, fx + b * 8 + cnt + t);
+            stage_f32_block_split(v, dst.col(t, b), dst.col(cnt + t, b), dst.factor(t, b), dst.factor(cnt + t, b));
         }
-        for (int it = tid; it < nb * 8; it += nthreads)
-            if ((it & 7) >= 2 * cnt) fx[it] = 0.0f;
+        for (int it = tid; it < nb * (8 - 2 * cnt); it += nthreads) {
+            const int b = it / (8 - 2 * cnt);
+            *dst.factor(2 * cnt + (it - b * (8 - 2 * cnt)), b) = 0.0f;
+        }
     }
 
     __device__ static void epilogue(const Params& p, int u, const Sums<1>& v, int lane) {

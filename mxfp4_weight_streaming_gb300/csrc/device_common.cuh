@@ -231,6 +231,16 @@ __device__ __forceinline__ float2 lds64f(uint32_t a) {
     return v;
 }
 
+__device__ __forceinline__ uint64_t lds64_pair(uint32_t a) {
+    uint64_t v;
+    asm volatile("ld.shared.b64 %0, [%1];" : "=l"(v) : "r"(a));
+    return v;
+}
+
+__device__ __forceinline__ void lds128_pairs(uint32_t a, uint64_t& lo, uint64_t& hi) {
+    asm volatile("ld.shared.v2.b64 {%0,%1}, [%2];" : "=l"(lo), "=l"(hi) : "r"(a));
+}
+
 __device__ __forceinline__ uint32_t lds_u8(uint32_t a) {
     uint32_t v;
     asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(a));
@@ -254,6 +264,69 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
         "{%10,%11,%12,%13};"
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+}
+
+// The two chained m16n8k16 products of one 32-block: A holds the 16 rows'
+// f16 weights (k permuted consistently with B), B the 8 columns' f16
+// activations, no accumulator input. The result comes back as the pairs
+// {d0, d1} (row g, columns 2t and 2t+1) and {d2, d3} (row g+8), each in
+// one 64-bit register pair for the packed f32x2 arithmetic below.
+__device__ __forceinline__ void mma_f16_k32(uint64_t& d01, uint64_t& d23, const uint32_t (&ga)[4],
+                                            const uint32_t (&gb)[4], const uint4& x) {
+    asm("{\n\t.reg .f32 t0, t1, t2, t3;\n\t"
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {t0,t1,t2,t3}, {%2,%3,%4,%5}, {%10,%11}, "
+        "{0f00000000,0f00000000,0f00000000,0f00000000};\n\t"
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {t0,t1,t2,t3}, {%6,%7,%8,%9}, {%12,%13}, "
+        "{t0,t1,t2,t3};\n\t"
+        "mov.b64 %0, {t0, t1};\n\t"
+        "mov.b64 %1, {t2, t3};\n\t}"
+        : "=l"(d01), "=l"(d23)
+        : "r"(ga[0]), "r"(gb[0]), "r"(ga[1]), "r"(gb[1]), "r"(ga[2]), "r"(gb[2]), "r"(ga[3]), "r"(gb[3]),
+          "r"(x.x), "r"(x.y), "r"(x.z), "r"(x.w));
+}
+
+// ------------------------------------------------------ packed f32 pairs
+// Blackwell issues two f32 multiplies or FMAs per instruction on a register
+// pair; a pair travels as one 64-bit value (low half = first element).
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+
+__device__ __forceinline__ float2 f32x2_unpack(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+
+__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+// Two E8M0 scale bytes (bits 0-7 and 8-15 of v) -> bf16x2 {2^(s0-127),
+// 2^(s1-127)}: bf16 holds every such power of two exactly (s = 0 is the
+// subnormal 2^-127).
+__device__ __forceinline__ uint32_t e8m0x2_to_bf16x2(uint32_t v) {
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.rn.bf16x2.ue8m0x2 %0, lo;\n\t}"
+        : "=r"(r)
+        : "r"(v));
+    return r;
 }
 
 // Four bytes of packed E2M1 pairs -> four f16x2 words (byte i -> out[i]);

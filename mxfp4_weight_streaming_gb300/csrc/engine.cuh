@@ -165,16 +165,23 @@ __device__ __forceinline__ void stage_f32_block_split(const float (&v)[32], uint
 // One K step of one unit: BOXES boxes of 16 rows x 256 K (8 blocks of 32;
 // fewer at the end of K), against the staged columns. Blocks are numbered
 // globally (scales) and relative to kblk0 (staged activations).
+//
+// Per block, the two MMAs give the exact-product sums d of the unscaled
+// codes and staged activations; the block's weight scale (per row) times
+// its activation factor (per column) is a power of two, and the pair
+// {d0, d1} (one row, two columns) is scaled and accumulated with one f32x2
+// multiply and one f32x2 FMA. acc[bx][n] = {{row g: col 2t, 2t+1}, {row g+8:
+// col 2t, 2t+1}} of n-tile n.
 template <int NT, int BOXES>
 __device__ __forceinline__ void consume_step(uint32_t slot, uint32_t box_stride, uint32_t sc, int nblk, int kb,
                                              int kblk0, int kblk1, int ncols, uint32_t xs, uint32_t xs_stride,
-                                             uint32_t fx, uint32_t fx_stride, float (&acc)[BOXES][NT][4], int lane) {
+                                             uint32_t fx, uint32_t fx_stride, uint64_t (&acc)[BOXES][NT][2],
+                                             int lane) {
     const int g = lane >> 2;
     const int tig = lane & 3;
     const int mi = lane >> 3;
     const int row = ((mi & 1) << 3) | (lane & 7);
     const int bsel = mi >> 1;
-    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int jp = 0; jp < 4; ++jp) {
         const int b_first = kb * 8 + 2 * jp;
@@ -190,31 +197,28 @@ __device__ __forceinline__ void consume_step(uint32_t slot, uint32_t box_stride,
             if (b >= kblk1) break;
             const int bl = b - kblk0;
             uint4 xv[NT];
-            float2 f[NT];
+            uint64_t F[NT];
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
-                const int col = g + 8 * n;
-                xv[n] = make_uint4(0, 0, 0, 0);
-                if (col < ncols) xv[n] = lds128(xs + col * xs_stride + bl * 64 + tig * 16);
-                f[n] = lds64f(fx + (tig + 4 * n) * fx_stride + bl * 8);
+                const int col = min(g + 8 * n, ncols - 1);  // see consume_step_full
+                xv[n] = lds128(xs + col * xs_stride + bl * 64 + tig * 16);
+                F[n] = lds64_pair(fx + (tig + 4 * n) * fx_stride + bl * 8);
             }
 #pragma unroll
             for (int bx = 0; bx < BOXES; ++bx) {
+                const uint32_t scb = sc + bx * 16 * nblk + b;
+                const uint32_t fw = e8m0x2_to_bf16x2(lds_u8(scb + g * nblk) | (lds_u8(scb + (g + 8) * nblk) << 8));
+                const float fw0 = __uint_as_float(fw << 16), fw1 = __uint_as_float(fw & 0xffff0000u);
+                const uint64_t W0 = f32x2_pack(fw0, fw0), W1 = f32x2_pack(fw1, fw1);
                 uint32_t ga[4], gb[4];
                 e2m1x8_to_f16x8(r[bx][2 * h], ga[0], ga[1], ga[2], ga[3]);
                 e2m1x8_to_f16x8(r[bx][2 * h + 1], gb[0], gb[1], gb[2], gb[3]);
-                const uint32_t scb = sc + bx * 16 * nblk;
-                const float fw0 = e8m0_to_float(lds_u8(scb + g * nblk + b));
-                const float fw1 = e8m0_to_float(lds_u8(scb + (g + 8) * nblk + b));
 #pragma unroll
                 for (int n = 0; n < NT; ++n) {
-                    float d[4];
-                    mma_f16_16816(d, ga[0], gb[0], ga[1], gb[1], xv[n].x, xv[n].y, zero4);
-                    mma_f16_16816(d, ga[2], gb[2], ga[3], gb[3], xv[n].z, xv[n].w, d);
-                    acc[bx][n][0] = fmaf(d[0], fw0 * f[n].x, acc[bx][n][0]);
-                    acc[bx][n][1] = fmaf(d[1], fw0 * f[n].y, acc[bx][n][1]);
-                    acc[bx][n][2] = fmaf(d[2], fw1 * f[n].x, acc[bx][n][2]);
-                    acc[bx][n][3] = fmaf(d[3], fw1 * f[n].y, acc[bx][n][3]);
+                    uint64_t d01, d23;
+                    mma_f16_k32(d01, d23, ga, gb, xv[n]);
+                    acc[bx][n][0] = f32x2_fma(d01, f32x2_mul(W0, F[n]), acc[bx][n][0]);
+                    acc[bx][n][1] = f32x2_fma(d23, f32x2_mul(W1, F[n]), acc[bx][n][1]);
                 }
             }
         }
@@ -222,19 +226,19 @@ __device__ __forceinline__ void consume_step(uint32_t slot, uint32_t box_stride,
 }
 
 // A full K step (all 8 blocks inside this CTA's range) with every shared
-// memory load of the step issued before the unpack / MMA chain, and the
-// scale bytes of 8 blocks read as one 8-byte word per row (needs K % 256
-// == 0 so the words are aligned).
+// memory load of the step issued before the unpack / MMA chain, the scale
+// bytes of 8 blocks read as one 8-byte word per row (needs K % 256 == 0 so
+// the words are aligned), and the activation factors of two blocks per
+// 16-byte load.
 template <int NT, int BOXES>
 __device__ __forceinline__ void consume_step_full(uint32_t slot, uint32_t box_stride, uint32_t sc, int nblk, int kb,
                                                   int kblk0, int ncols, uint32_t xs, uint32_t xs_stride, uint32_t fx,
-                                                  uint32_t fx_stride, float (&acc)[BOXES][NT][4], int lane) {
+                                                  uint32_t fx_stride, uint64_t (&acc)[BOXES][NT][2], int lane) {
     const int g = lane >> 2;
     const int tig = lane & 3;
     const int mi = lane >> 3;
     const int row = ((mi & 1) << 3) | (lane & 7);
     const int bsel = mi >> 1;
-    const float zero4[4] = {0.f, 0.f, 0.f, 0.f};
     uint32_t r[BOXES][4][4];
 #pragma unroll
     for (int bx = 0; bx < BOXES; ++bx)
@@ -251,43 +255,43 @@ __device__ __forceinline__ void consume_step_full(uint32_t slot, uint32_t box_st
     }
     const int bl0 = kb * 8 - kblk0;
     // Per-lane bases of this step; the 8 blocks are immediate offsets.
+    // A lane whose token column does not exist (every unit has at least one)
+    // reads the last real column instead: that column of the MMA output only
+    // meets zero factors, so it adds nothing, and the load needs no branch.
     uint32_t xb[NT], fb[NT];
-    bool has[NT];
 #pragma unroll
     for (int n = 0; n < NT; ++n) {
-        xb[n] = xs + (g + 8 * n) * xs_stride + bl0 * 64 + tig * 16;
+        xb[n] = xs + min(g + 8 * n, ncols - 1) * xs_stride + bl0 * 64 + tig * 16;
         fb[n] = fx + (tig + 4 * n) * fx_stride + bl0 * 8;
-        has[n] = g + 8 * n < ncols;
     }
+    uint64_t Fe[NT], Fo[NT];
 #pragma unroll
     for (int blk = 0; blk < 8; ++blk) {
         uint4 xv[NT];
-        float2 f[NT];
 #pragma unroll
         for (int n = 0; n < NT; ++n) {
-            xv[n] = make_uint4(0, 0, 0, 0);
-            if (has[n]) xv[n] = lds128(xb[n] + blk * 64);
-            f[n] = lds64f(fb[n] + blk * 8);
+            xv[n] = lds128(xb[n] + blk * 64);
+            if ((blk & 1) == 0) lds128_pairs(fb[n] + blk * 8, Fe[n], Fo[n]);
         }
         const int jp = blk >> 1, h = blk & 1;
 #pragma unroll
         for (int bx = 0; bx < BOXES; ++bx) {
+            // Byte (blk & 3) of both rows' scale words -> bytes 0 and 1.
             const uint32_t w0 = blk < 4 ? s0[bx].x : s0[bx].y;
             const uint32_t w1 = blk < 4 ? s1[bx].x : s1[bx].y;
-            const float fw0 = e8m0_to_float((w0 >> (8 * (blk & 3))) & 0xffu);
-            const float fw1 = e8m0_to_float((w1 >> (8 * (blk & 3))) & 0xffu);
+            const uint32_t fw = e8m0x2_to_bf16x2(prmt(w0, w1, (blk & 3) | ((4 + (blk & 3)) << 4)));
+            const float fw0 = __uint_as_float(fw << 16), fw1 = __uint_as_float(fw & 0xffff0000u);
+            const uint64_t W0 = f32x2_pack(fw0, fw0), W1 = f32x2_pack(fw1, fw1);
             uint32_t ga[4], gb[4];
             e2m1x8_to_f16x8(r[bx][jp][2 * h], ga[0], ga[1], ga[2], ga[3]);
             e2m1x8_to_f16x8(r[bx][jp][2 * h + 1], gb[0], gb[1], gb[2], gb[3]);
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
-                float d[4];
-                mma_f16_16816(d, ga[0], gb[0], ga[1], gb[1], xv[n].x, xv[n].y, zero4);
-                mma_f16_16816(d, ga[2], gb[2], ga[3], gb[3], xv[n].z, xv[n].w, d);
-                acc[bx][n][0] = fmaf(d[0], fw0 * f[n].x, acc[bx][n][0]);
-                acc[bx][n][1] = fmaf(d[1], fw0 * f[n].y, acc[bx][n][1]);
-                acc[bx][n][2] = fmaf(d[2], fw1 * f[n].x, acc[bx][n][2]);
-                acc[bx][n][3] = fmaf(d[3], fw1 * f[n].y, acc[bx][n][3]);
+                const uint64_t F = h ? Fo[n] : Fe[n];
+                uint64_t d01, d23;
+                mma_f16_k32(d01, d23, ga, gb, xv[n]);
+                acc[bx][n][0] = f32x2_fma(d01, f32x2_mul(W0, F), acc[bx][n][0]);
+                acc[bx][n][1] = f32x2_fma(d23, f32x2_mul(W1, F), acc[bx][n][1]);
             }
         }
     }
@@ -424,6 +428,14 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
     int ncols = 0;
     uint32_t xphase = 0;
     uint32_t i = warp;
+    // This warp's steps are i = warp, warp + NCW, ...; step i is step
+    // `within` of stage i / spb, which sits in ring slot stage % nslot.
+    const uint32_t ring = S.base + L.ring;
+    const uint32_t box_stride = spb * kBoxBytes;
+    const uint32_t adv_stage = P::NCW / spb, adv_within = P::NCW - (P::NCW / spb) * spb;
+    uint32_t within = i % spb;
+    uint32_t slot = (i / spb) % L.nslot;
+    uint32_t phase = ((i / spb) / L.nslot) & 1u;
     for (int u = pl.u0; u < pl.u1; ++u) {
         const uint32_t uu = u - pl.u0;
         const int chunk = P::chunk_of(p, u);
@@ -447,20 +459,17 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
         const uint32_t ss = uu % L.nss;
         if (!warp_wait(bars.sfull(ss), (uu / L.nss) & 1, S.wait)) return;
         const uint32_t sc = scb + ss * L.ss_bytes;
-        float acc[BOXES][NT][4];
+        uint64_t acc[BOXES][NT][2];
 #pragma unroll
         for (int bx = 0; bx < BOXES; ++bx)
 #pragma unroll
-            for (int n = 0; n < NT; ++n) acc[bx][n][0] = acc[bx][n][1] = acc[bx][n][2] = acc[bx][n][3] = 0.f;
+            for (int n = 0; n < NT; ++n) acc[bx][n][0] = acc[bx][n][1] = 0ull;  // +0.0f pairs
         const uint32_t ib = uu * nkbc;
         for (; i < ib + nkbc; i += P::NCW) {
             // Steps are grouped in stages of spb (spb divides the steps of a
             // unit, so a stage never straddles two units).
-            const uint32_t stage = i / spb;
-            const uint32_t slot = stage % L.nslot;
-            if (!warp_wait(bars.full(slot), (stage / L.nslot) & 1, S.wait)) return;
-            const uint32_t box_stride = spb * kBoxBytes;
-            const uint32_t step_smem = S.base + L.ring + slot * stage_bytes + (i - stage * spb) * kBoxBytes;
+            if (!warp_wait(bars.full(slot), phase, S.wait)) return;
+            const uint32_t step_smem = ring + slot * stage_bytes + within * kBoxBytes;
             const int kb = pl.kb0 + static_cast<int>(i - ib);
             if (fast_steps && kb * 8 + 8 <= pl.kblk1)
                 consume_step_full<NT, BOXES>(step_smem, box_stride, sc, p.nblk, kb, pl.kblk0, ncols, xs_s,
@@ -470,6 +479,19 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
                                         L.xs_stride, fx_s, L.fx_stride, acc, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(bars.empty(slot));
+            // Next step of this warp: i + NCW, i.e. (stage, within) advanced
+            // without a division.
+            within += adv_within;
+            uint32_t ds = adv_stage;
+            if (within >= spb) {
+                within -= spb;
+                ++ds;
+            }
+            slot += ds;
+            while (slot >= L.nslot) {
+                slot -= L.nslot;
+                phase ^= 1u;
+            }
         }
         const uint32_t rb = uu & 1;
         if (!warp_wait(bars.rempty(rb), ((uu >> 1) & 1) ^ 1, S.wait)) return;
@@ -480,10 +502,11 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
 #pragma unroll
             for (int n = 0; n < NT; ++n) {
                 float* Rb = R + (bx * 8 * NT + 8 * n + 2 * tig) * kRedStride;
-                Rb[g] = acc[bx][n][0];
-                Rb[kRedStride + g] = acc[bx][n][1];
-                Rb[g + 8] = acc[bx][n][2];
-                Rb[kRedStride + g + 8] = acc[bx][n][3];
+                const float2 a01 = f32x2_unpack(acc[bx][n][0]), a23 = f32x2_unpack(acc[bx][n][1]);
+                Rb[g] = a01.x;
+                Rb[kRedStride + g] = a01.y;
+                Rb[g + 8] = a23.x;
+                Rb[kRedStride + g + 8] = a23.y;
             }
         __syncwarp();
         if (lane == 0) {

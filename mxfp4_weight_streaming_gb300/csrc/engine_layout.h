@@ -13,7 +13,7 @@ struct SmemLayout {
     uint32_t xs;        // staged activations, f16 [xcols][blocks][32], column stride xs_stride
     uint32_t fx;        // activation block factors, f32 [4*NT column pairs][blocks][2], stride fx_stride
     uint32_t xs_stride; // bytes per staged column (blocks*64 + 16: the pad spreads columns over banks)
-    uint32_t fx_stride; // bytes per column pair of factors (blocks*8 + 16)
+    uint32_t fx_stride; // bytes per column pair of factors (blocks*8 rounded up to 16, + 16)
     uint32_t sc;        // scale ring: nss slots of ss_bytes
     uint32_t nss;
     uint32_t ss_bytes;  // one unit's scales: BOXES x 16 x K/32 bytes
@@ -43,7 +43,7 @@ inline bool plan_layout(int nt, int boxes, int nblk, int nblk_all, int xcols, in
     const int nkb = (nblk + 7) / 8;
     const uint32_t slot_bytes = 2048u * boxes * steps;
     const uint32_t xs_stride = static_cast<uint32_t>(nblk) * 64 + 16;
-    const uint32_t fx_stride = static_cast<uint32_t>(nblk) * 8 + 16;
+    const uint32_t fx_stride = al(static_cast<uint32_t>(nblk) * 8, 16) + 16;  // 16-byte loads of 2 blocks
     const uint32_t xs_bytes = static_cast<uint32_t>(xcols) * xs_stride;
     const uint32_t fx_bytes = static_cast<uint32_t>(4 * nt) * fx_stride;
     const uint32_t ss_bytes = al(static_cast<uint32_t>(boxes) * 16 * nblk_all, 16);

@@ -39,10 +39,16 @@ struct DenseProblem {
                                  int nthreads) {
         const int T = p.T;
         const int nb = kblk1 - kblk0;
-        const int items = nb * T;
-        for (int it = tid; it < items; it += nthreads) {
-            const int b = it / T;
-            const int t = it - b * T;
+        // Items (block b, token t) = tid, tid + nthreads, ...; (b, t) advance
+        // without a division per item.
+        const int db = nthreads / T, dt = nthreads - (nthreads / T) * T;
+        int b = tid / T, t = tid - (tid / T) * T;
+        for (; b < nb; b += db, t += dt) {
+            if (t >= T) {
+                t -= T;
+                ++b;
+                if (b >= nb) break;
+            }
             const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * p.K + (size_t)(kblk0 + b) * 32);
             uint4 v[4];
 #pragma unroll

@@ -91,6 +91,53 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
     }
 }
 
+// Waits until the shared word at addr holds want (written by another warp of
+// the CTA). Same limits as mbar_wait.
+__device__ __forceinline__ uint32_t lds_u32_volatile(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void sts_u32_volatile(uint32_t a, uint32_t v) {
+    asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ bool wait_shared_value(uint32_t addr, uint32_t want, const WaitCtx& w) {
+    if (lds_u32_volatile(addr) == want) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (*w.abort) return false;
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i) {
+            __nanosleep(32);
+            if (lds_u32_volatile(addr) == want) return true;
+        }
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            record_timeout(w);
+            return false;
+        }
+    }
+}
+
+// Waits until the shared counter at addr is >= want.
+__device__ __forceinline__ bool wait_shared_at_least(uint32_t addr, uint32_t want, const WaitCtx& w) {
+    if (lds_u32_volatile(addr) >= want) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (*w.abort) return false;
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i) {
+            __nanosleep(32);
+            if (lds_u32_volatile(addr) >= want) return true;
+        }
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            record_timeout(w);
+            return false;
+        }
+    }
+}
+
 // ------------------------------------------- programmatic dependent launch
 // Lets the next kernel of the stream be scheduled before this one ends (its
 // CTAs become resident as SMs free up).
@@ -139,6 +186,17 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+
+// Arrive on an mbarrier of another CTA of the cluster without ordering
+// this thread's memory accesses (for "buffer free again" signals whose
+// reads have already completed).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Makes this thread's earlier writes (and those ordered before them, e.g.
+// by a warp barrier) visible cluster-wide before its later writes.
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
 
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
     uint32_t ok;
@@ -209,6 +267,20 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
+// The same bulk copy with the default L2 policy (for data that many CTAs
+// read, such as activations).
+__device__ __forceinline__ void bulk_load_plain(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Orders this thread's earlier generic-proxy accesses to shared memory
+// before its later bulk (async-proxy) copies into it.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---------------------------------------------------- shared-memory loads
 // Explicit ld.shared on 32-bit shared addresses (a generic pointer into
 // shared memory would go through the slower generic path). Volatile so they
@@ -217,6 +289,10 @@ __device__ __forceinline__ uint4 lds128(uint32_t a) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
     return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
 }
 
 __device__ __forceinline__ uint2 lds64(uint32_t a) {

@@ -47,15 +47,28 @@ struct Roles {
 constexpr int kBoxBytes = 2048;  // 16 rows x 128 bytes = 16 rows x 256 K values
 constexpr int kRedStride = 20;   // floats per column row of the reduction area (16 + 4 pad)
 
+// mbarriers and tag words of one CTA (shared addresses), in the order the
+// layout plans them.
 struct Bars {
     uint32_t base;
-    uint32_t nslot, nss;
+    uint32_t nslot, nss, nrb;
+    uint32_t tags;
     __device__ uint32_t full(uint32_t s) const { return base + 8 * s; }
     __device__ uint32_t empty(uint32_t s) const { return base + 8 * (nslot + s); }
     __device__ uint32_t sfull(uint32_t s) const { return base + 8 * (2 * nslot + s); }
     __device__ uint32_t sempty(uint32_t s) const { return base + 8 * (2 * nslot + nss + s); }
     __device__ uint32_t rfull(uint32_t b) const { return base + 8 * (2 * nslot + 2 * nss + b); }
-    __device__ uint32_t rempty(uint32_t b) const { return base + 8 * (2 * nslot + 2 * nss + 2 + b); }
+    __device__ uint32_t cfull(uint32_t b) const { return base + 8 * (2 * nslot + 2 * nss + nrb + b); }
+    __device__ uint32_t cempty(uint32_t b) const { return base + 8 * (2 * nslot + 2 * nss + nrb + 2 + b); }
+    // xbar(0), xbar(1): all consumers before / after staging; xbar(2): the
+    // bulk copies of raw activations have landed.
+    __device__ uint32_t xbar(uint32_t b) const { return base + 8 * (2 * nslot + 2 * nss + nrb + 4 + b); }
+    __device__ uint32_t abort_flag() const { return base + 8 * (2 * nslot + 2 * nss + nrb + 7); }
+    // Stage last issued into ring slot s; unit last issued into scale slot s;
+    // number of units the reducer has finished reading.
+    __device__ uint32_t ring_tag(uint32_t s) const { return tags + 4 * s; }
+    __device__ uint32_t scale_tag(uint32_t s) const { return tags + 4 * (nslot + s); }
+    __device__ uint32_t progress() const { return tags + 4 * (nslot + nss); }
 };
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx& w) {
@@ -159,6 +172,52 @@ __device__ __forceinline__ void stage_f32_block_split(const float (&v)[32], uint
     const float f = exp2_int(-c);
     *fx_hi = f;
     *fx_lo = f;
+}
+
+// ------------------------------------------------------------------------
+// Activation staging by bulk copy: for problems whose staged columns are
+// bf16 rows of K values (P::kBulkStage), one thread copies each column's
+// K range [kblk0*32, kblk1*32) straight into its staged column (the byte
+// layout is the same: 64 bytes per 32-block), then every consumer thread
+// converts blocks in place. Only shared-memory latency is on the path,
+// instead of one dependent global load per block and thread.
+template <class P>
+__device__ __forceinline__ bool stage_bulk(const typename P::Params& p, int chunk, int kblk0, int kblk1,
+                                           const StageDst& dst, uint32_t xs_s, uint32_t xfull, uint32_t parity,
+                                           const WaitCtx& wc, int tid, int nthreads) {
+    constexpr int kCols = 8 * P::NT;  // staged tile width (columns)
+    const int ncol = P::stage_cols(p, chunk);
+    const int nb = kblk1 - kblk0;
+    if (tid == 0) {
+        fence_proxy_async_shared();  // earlier reads / writes of the columns come first
+        mbar_arrive_expect_tx(xfull, static_cast<uint32_t>(ncol * nb * 64));
+        if (nb > 0)
+            for (int t = 0; t < ncol; ++t)
+                bulk_load_plain(xs_s + t * dst.xs_stride, P::stage_row(p, chunk, t) + static_cast<size_t>(kblk0) * 64,
+                                static_cast<uint32_t>(nb * 64), xfull);
+    }
+    if (!__all_sync(0xffffffffu, mbar_wait(xfull, parity, wc))) return false;
+    for (int it = tid; it < ncol * nb; it += nthreads) {
+        const int t = it / nb;
+        const int b = it - t * nb;
+        const uint32_t a = xs_s + t * dst.xs_stride + b * 64;
+        uint32_t w[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 v = lds128(a + 16 * q);
+            w[4 * q] = v.x;
+            w[4 * q + 1] = v.y;
+            w[4 * q + 2] = v.z;
+            w[4 * q + 3] = v.w;
+        }
+        stage_bf16_block(w, dst.col(t, b), dst.factor(t, b));
+    }
+    // Factors of the unused columns of the tile are zero.
+    for (int it = tid; it < nb * (kCols - ncol); it += nthreads) {
+        const int b = it / (kCols - ncol);
+        *dst.factor(ncol + (it - b * (kCols - ncol)), b) = 0.0f;
+    }
+    return true;
 }
 
 // ------------------------------------------------------------------------
@@ -319,8 +378,6 @@ struct Smem {
     uint8_t* gbase;
     SmemLayout L;
     Bars bars;
-    uint32_t cbars;  // cluster barriers: cfull[2], cempty[2]
-    uint32_t xbars;  // consumer barriers around activation staging: [2]
     WaitCtx wait;
 };
 
@@ -338,6 +395,7 @@ __device__ void producer_role(const typename P::Params& p, const Smem& S, const 
     const uint32_t stage_bytes = spb * BOXES * kBoxBytes;
     const uint32_t scale_bytes = 16u * static_cast<uint32_t>(p.nblk);
     const int nkbc = pl.kb1 - pl.kb0;
+    if (nkbc <= 0) return;  // a cluster rank with no part of K: nothing to stream
     const uint64_t policy = l2_evict_first_policy();
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
     bool ok = true;
@@ -349,6 +407,7 @@ __device__ void producer_role(const typename P::Params& p, const Smem& S, const 
             ok = false;
             break;
         }
+        sts_u32_volatile(bars.scale_tag(ss), uu);  // the slot now belongs to unit uu
         // Scale rows of the unit: a bulk copy of the 16-byte-aligned part, and
         // (only for a tail row group) the last few bytes stored by this lane.
         const uint32_t bytes = static_cast<uint32_t>(P::unit_rows(p, u)) * static_cast<uint32_t>(p.nblk);
@@ -376,6 +435,10 @@ __device__ void producer_role(const typename P::Params& p, const Smem& S, const 
                 ok = false;
                 break;
             }
+            // The slot now belongs to stage `staged`: its previous stage has
+            // been consumed, so a consumer that sees this tag can wait on the
+            // slot's full barrier without mistaking an older phase for it.
+            sts_u32_volatile(bars.ring_tag(slot), staged);
             mbar_arrive_expect_tx(bars.full(slot), stage_bytes);
             // Stage layout: [box][step][16 rows][128 B], 128-byte swizzle.
             const uint32_t sbase = S.base + L.ring + slot * stage_bytes;
@@ -417,6 +480,7 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
     const SmemLayout& L = S.L;
     const Bars& bars = S.bars;
     const uint32_t spb = L.steps;
+    const uint32_t G = L.group;
     const uint32_t stage_bytes = spb * BOXES * kBoxBytes;
     uint8_t* xs = S.gbase + L.xs;
     float* fx = reinterpret_cast<float*>(S.gbase + L.fx);
@@ -427,15 +491,21 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
     int cur_chunk = -1;
     int ncols = 0;
     uint32_t xphase = 0;
-    uint32_t i = warp;
-    // This warp's steps are i = warp, warp + NCW, ...; step i is step
-    // `within` of stage i / spb, which sits in ring slot stage % nslot.
+    // The CTA's K steps, unit after unit, are cut into chunks of G steps
+    // (G divides the stage size spb, which divides a unit's steps, so a chunk
+    // never straddles two stages or two units). This warp takes chunks c =
+    // warp, warp + NCW, ...; chunk c is chunk `within` of stage c / cps,
+    // which sits in ring slot stage % nslot.
+    const uint32_t cps = spb / G;
+    const uint32_t cpu = static_cast<uint32_t>(nkbc) / G;
     const uint32_t ring = S.base + L.ring;
     const uint32_t box_stride = spb * kBoxBytes;
-    const uint32_t adv_stage = P::NCW / spb, adv_within = P::NCW - (P::NCW / spb) * spb;
-    uint32_t within = i % spb;
-    uint32_t slot = (i / spb) % L.nslot;
-    uint32_t phase = ((i / spb) / L.nslot) & 1u;
+    const uint32_t adv_stage = P::NCW / cps, adv_within = P::NCW - (P::NCW / cps) * cps;
+    uint32_t c = warp;
+    uint32_t within = c % cps;
+    uint32_t stage = c / cps;
+    uint32_t slot = stage % L.nslot;
+    uint32_t phase = (stage / L.nslot) & 1u;
     for (int u = pl.u0; u < pl.u1; ++u) {
         const uint32_t uu = u - pl.u0;
         const int chunk = P::chunk_of(p, u);
@@ -445,69 +515,97 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
             // and the new ones are complete before anyone reads them. The
             // barriers are mbarriers so a wait can give up instead of hang.
             __syncwarp();
-            if (lane == 0) mbar_arrive(S.xbars);
-            if (!warp_wait(S.xbars, xphase & 1, S.wait)) return;
-            P::stage(p, chunk, pl.kblk0, pl.kblk1, StageDst{xs, reinterpret_cast<uint8_t*>(fx), L.xs_stride, L.fx_stride},
-                     warp * 32 + lane, Roles<P>::kConsumerThreads);
+            if (lane == 0) mbar_arrive(bars.xbar(0));
+            if (!warp_wait(bars.xbar(0), xphase & 1, S.wait)) return;
+            const StageDst dst{xs, reinterpret_cast<uint8_t*>(fx), L.xs_stride, L.fx_stride};
+            if constexpr (P::kBulkStage) {
+                if (!stage_bulk<P>(p, chunk, pl.kblk0, pl.kblk1, dst, xs_s, bars.xbar(2), xphase & 1, S.wait,
+                                   warp * 32 + lane, Roles<P>::kConsumerThreads))
+                    return;
+            } else {
+                P::stage(p, chunk, pl.kblk0, pl.kblk1, dst, warp * 32 + lane, Roles<P>::kConsumerThreads);
+            }
             __syncwarp();
-            if (lane == 0) mbar_arrive(S.xbars + 8);
-            if (!warp_wait(S.xbars + 8, xphase & 1, S.wait)) return;
+            if (lane == 0) mbar_arrive(bars.xbar(1));
+            if (!warp_wait(bars.xbar(1), xphase & 1, S.wait)) return;
             ++xphase;
             cur_chunk = chunk;
             ncols = P::ncols(p, chunk);
         }
         const uint32_t ss = uu % L.nss;
-        if (!warp_wait(bars.sfull(ss), (uu / L.nss) & 1, S.wait)) return;
-        const uint32_t sc = scb + ss * L.ss_bytes;
+        const uint32_t cb = uu * cpu;  // first chunk of this unit
+        // A warp owns chunks of this unit iff its next chunk lies inside it;
+        // its partial goes to slot c - cb (< NCW, since its previous chunk
+        // lies before the unit).
+        // Only owners take part in the unit: they wait for its scales, hand
+        // their partial to the reducer and release the scale slot.
+        if (c >= cb + cpu) continue;
+        const uint32_t jred = c - cb;
         uint64_t acc[BOXES][NT][2];
 #pragma unroll
         for (int bx = 0; bx < BOXES; ++bx)
 #pragma unroll
             for (int n = 0; n < NT; ++n) acc[bx][n][0] = acc[bx][n][1] = 0ull;  // +0.0f pairs
-        const uint32_t ib = uu * nkbc;
-        for (; i < ib + nkbc; i += P::NCW) {
-            // Steps are grouped in stages of spb (spb divides the steps of a
-            // unit, so a stage never straddles two units).
-            if (!warp_wait(bars.full(slot), phase, S.wait)) return;
-            const uint32_t step_smem = ring + slot * stage_bytes + within * kBoxBytes;
-            const int kb = pl.kb0 + static_cast<int>(i - ib);
-            if (fast_steps && kb * 8 + 8 <= pl.kblk1)
-                consume_step_full<NT, BOXES>(step_smem, box_stride, sc, p.nblk, kb, pl.kblk0, ncols, xs_s,
-                                             L.xs_stride, fx_s, L.fx_stride, acc, lane);
-            else
-                consume_step<NT, BOXES>(step_smem, box_stride, sc, p.nblk, kb, pl.kblk0, pl.kblk1, ncols, xs_s,
-                                        L.xs_stride, fx_s, L.fx_stride, acc, lane);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bars.empty(slot));
-            // Next step of this warp: i + NCW, i.e. (stage, within) advanced
-            // without a division.
-            within += adv_within;
-            uint32_t ds = adv_stage;
-            if (within >= spb) {
-                within -= spb;
-                ++ds;
-            }
-            slot += ds;
-            while (slot >= L.nslot) {
-                slot -= L.nslot;
-                phase ^= 1u;
+        {
+            // This warp may be several units ahead of the scale ring: the tag
+            // says the slot holds this unit's scales (or is being filled).
+            if (!__all_sync(0xffffffffu, wait_shared_value(bars.scale_tag(ss), uu, S.wait))) return;
+            if (!warp_wait(bars.sfull(ss), (uu / L.nss) & 1, S.wait)) return;
+            const uint32_t sc = scb + ss * L.ss_bytes;
+            for (; c < cb + cpu; c += P::NCW) {
+                // A warp may run several stages ahead of the ring: first wait
+                // until the producer has claimed the slot for this stage, so
+                // the parity wait below refers to this stage's phase.
+                if (!__all_sync(0xffffffffu, wait_shared_value(bars.ring_tag(slot), stage, S.wait))) return;
+                if (!warp_wait(bars.full(slot), phase, S.wait)) return;
+                uint32_t step_smem = ring + slot * stage_bytes + within * G * kBoxBytes;
+                int kb = pl.kb0 + static_cast<int>((c - cb) * G);
+                for (uint32_t st = 0; st < G; ++st, ++kb, step_smem += kBoxBytes) {
+                    if (fast_steps && kb * 8 + 8 <= pl.kblk1)
+                        consume_step_full<NT, BOXES>(step_smem, box_stride, sc, p.nblk, kb, pl.kblk0, ncols, xs_s,
+                                                     L.xs_stride, fx_s, L.fx_stride, acc, lane);
+                    else
+                        consume_step<NT, BOXES>(step_smem, box_stride, sc, p.nblk, kb, pl.kblk0, pl.kblk1, ncols,
+                                                xs_s, L.xs_stride, fx_s, L.fx_stride, acc, lane);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.empty(slot));
+                // Next chunk of this warp: c + NCW, i.e. (stage, within)
+                // advanced without a division.
+                within += adv_within;
+                uint32_t ds = adv_stage;
+                if (within >= cps) {
+                    within -= cps;
+                    ++ds;
+                }
+                stage += ds;
+                slot += ds;
+                while (slot >= L.nslot) {
+                    slot -= L.nslot;
+                    phase ^= 1u;
+                }
             }
         }
-        const uint32_t rb = uu & 1;
-        if (!warp_wait(bars.rempty(rb), ((uu >> 1) & 1) ^ 1, S.wait)) return;
-        float* R = redw + (rb * P::NCW + warp) * kRedWarpFloats;
-        const int g = lane >> 2, tig = lane & 3;
+        // Reduction buffer uu % nrb is free once the reducer has finished
+        // unit uu - nrb.
+        const uint32_t rb = uu % L.nrb;
+        if (!__all_sync(0xffffffffu, wait_shared_at_least(bars.progress(), uu + 1 - min(uu + 1, L.nrb), S.wait)))
+            return;
+        {
+            float* R = redw + (rb * L.nred + jred) * kRedWarpFloats;
+            const int g = lane >> 2, tig = lane & 3;
 #pragma unroll
-        for (int bx = 0; bx < BOXES; ++bx)
+            for (int bx = 0; bx < BOXES; ++bx)
 #pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                float* Rb = R + (bx * 8 * NT + 8 * n + 2 * tig) * kRedStride;
-                const float2 a01 = f32x2_unpack(acc[bx][n][0]), a23 = f32x2_unpack(acc[bx][n][1]);
-                Rb[g] = a01.x;
-                Rb[kRedStride + g] = a01.y;
-                Rb[g + 8] = a23.x;
-                Rb[kRedStride + g + 8] = a23.y;
-            }
+                for (int n = 0; n < NT; ++n) {
+                    float* Rb = R + (bx * 8 * NT + 8 * n + 2 * tig) * kRedStride;
+                    const float2 a01 = f32x2_unpack(acc[bx][n][0]), a23 = f32x2_unpack(acc[bx][n][1]);
+                    Rb[g] = a01.x;
+                    Rb[kRedStride + g] = a01.y;
+                    Rb[g + 8] = a23.x;
+                    Rb[kRedStride + g + 8] = a23.y;
+                }
+        }
         __syncwarp();
         if (lane == 0) {
             mbar_arrive(bars.rfull(rb));
@@ -527,54 +625,76 @@ __device__ void reducer_role(const typename P::Params& p, const Smem& S, const P
     const float* red = reinterpret_cast<const float*>(S.gbase + L.red);
     float* fin = reinterpret_cast<float*>(S.gbase + L.fin);
     const float* recv = reinterpret_cast<const float*>(S.gbase + L.recv);
-    const uint32_t cfull0 = S.cbars, cempty0 = S.cbars + 16;
+    // Partials per unit: one per consumer warp that owns chunks of it.
+    const int cpu = (pl.kb1 - pl.kb0) / static_cast<int>(L.group);
+    const int nown = cpu < P::NCW ? cpu : P::NCW;
     pdl_wait_previous();  // outputs may be read or written by the previous kernel
+    uint32_t b = 0, bphase = 0;  // reduction buffer uu % nrb and its phase
     for (int u = pl.u0; u < pl.u1; ++u) {
         const uint32_t uu = u - pl.u0;
-        const uint32_t rb = uu & 1;
-        if (!warp_wait(bars.rfull(rb), (uu >> 1) & 1, S.wait)) return;
+        const uint32_t rb = uu & 1;  // fin buffer and cluster slot
+        if (nown > 0 && !warp_wait(bars.rfull(b), bphase, S.wait)) return;
         const int ncols = P::ncols(p, P::chunk_of(p, u));
-        // CTA-local sums over the consumer warps, fixed order.
-        const float* R = red + rb * P::NCW * kRedWarpFloats;
+        // CTA-local sums over the unit's partials, in K order (slot j holds
+        // the chunks j, j + NCW, ... of the unit).
+        const float* R = red + b * L.nred * kRedWarpFloats;
         float* F = fin + rb * kFin;
-        for (int e = lane; e < BOXES * ncols * 16; e += 32) {
-            const int bx = e / (ncols * 16);
-            const int rem = e - bx * ncols * 16;
-            const int col = rem >> 4, r = rem & 15;
-            float s = 0.f;
 #pragma unroll
-            for (int w = 0; w < P::NCW; ++w) s += R[w * kRedWarpFloats + (bx * 8 * NT + col) * kRedStride + r];
-            F[(bx * 8 * NT + col) * 16 + r] = s;
-        }
+        for (int bx = 0; bx < BOXES; ++bx)
+            for (int e = lane; e < ncols * 16; e += 32) {
+                const int idx = bx * 8 * NT + (e >> 4), r = e & 15;
+                float s = 0.f;
+                for (int j = 0; j < nown; ++j) s += R[j * kRedWarpFloats + idx * kRedStride + r];
+                F[idx * 16 + r] = s;
+            }
+        // Buffer b may be refilled (by the owners of unit uu + nrb) once every
+        // lane's reads of it are done.
         __syncwarp();
-        if (lane == 0) mbar_arrive(bars.rempty(rb));
+        __threadfence_block();
+        if (lane == 0) sts_u32_volatile(bars.progress(), uu + 1);
+        if (++b == L.nrb) {
+            b = 0;
+            bphase ^= 1u;
+        }
         if (pl.cl > 1) {
             if (pl.rank != 0) {
                 // Send this CTA's part of K to the leader, in its rank's slot.
-                if (!__all_sync(0xffffffffu, mbar_wait_cluster(cempty0 + 8 * rb, ((uu >> 1) & 1) ^ 1, S.wait)))
-                    return;
+                // One lane waits (cluster-scope acquire), the warp follows.
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait_cluster(bars.cempty(rb), ((uu >> 1) & 1) ^ 1, S.wait);
+                if (!__shfl_sync(0xffffffffu, ok, 0)) return;
                 const uint32_t dst = map_to_rank(S.base + L.recv + ((rb * (pl.cl - 1) + pl.rank - 1) * kFin) * 4, 0);
-                for (int e = lane; e < BOXES * ncols * 16; e += 32) {
-                    const int bx = e / (ncols * 16);
-                    const int rem = e - bx * ncols * 16;
-                    const int idx = (bx * 8 * NT + (rem >> 4)) * 16 + (rem & 15);
-                    st_cluster_f32(dst + idx * 4, F[idx]);
+#pragma unroll
+                for (int bx = 0; bx < BOXES; ++bx)
+                    for (int e = lane; e < ncols * 16; e += 32) {
+                        const int idx = bx * 8 * NT * 16 + e;
+                        st_cluster_f32(dst + idx * 4, F[idx]);
+                    }
+                // All lanes' remote stores, then one cluster-scope release.
+                __syncwarp();
+                if (lane == 0) {
+                    fence_acq_rel_cluster();
+                    mbar_arrive_remote(map_to_rank(bars.cfull(rb), 0));
                 }
-                mbar_arrive_remote(map_to_rank(cfull0 + 8 * rb, 0));
                 continue;
             }
             // Leader: add the other ranks' parts in rank order.
-            if (!__all_sync(0xffffffffu, mbar_wait_cluster(cfull0 + 8 * rb, (uu >> 1) & 1, S.wait))) return;
-            for (int e = lane; e < BOXES * ncols * 16; e += 32) {
-                const int bx = e / (ncols * 16);
-                const int rem = e - bx * ncols * 16;
-                const int idx = (bx * 8 * NT + (rem >> 4)) * 16 + (rem & 15);
-                float s = F[idx];
-                for (uint32_t q = 0; q + 1 < pl.cl; ++q) s += recv[(rb * (pl.cl - 1) + q) * kFin + idx];
-                F[idx] = s;
-            }
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait_cluster(bars.cfull(rb), (uu >> 1) & 1, S.wait);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+#pragma unroll
+            for (int bx = 0; bx < BOXES; ++bx)
+                for (int e = lane; e < ncols * 16; e += 32) {
+                    const int idx = bx * 8 * NT * 16 + e;
+                    float s = F[idx];
+                    for (uint32_t q = 0; q + 1 < pl.cl; ++q) s += recv[(rb * (pl.cl - 1) + q) * kFin + idx];
+                    F[idx] = s;
+                }
             __syncwarp();
-            for (uint32_t q = 1; q < pl.cl; ++q) mbar_arrive_remote(map_to_rank(cempty0 + 8 * rb, q));
+            // The other ranks may refill slot rb: every lane's reads of it
+            // are done (their values are in F).
+            if (lane == 0)
+                for (uint32_t q = 1; q < pl.cl; ++q) mbar_arrive_remote_relaxed(map_to_rank(bars.cempty(rb), q));
         }
         P::epilogue(p, u, Sums<NT>{F}, lane);
         __syncwarp();
@@ -608,10 +728,8 @@ __global__ void __launch_bounds__(Roles<P>::kThreads, 1)
     S.base = (raw + 1023u) & ~1023u;
     S.gbase = smem_raw + (S.base - raw);
     S.L = p.layout;
-    S.bars = Bars{S.base + S.L.bars, S.L.nslot, S.L.nss};
-    S.cbars = S.base + S.L.bars + 8 * (2 * S.L.nslot + 2 * S.L.nss + 4);
-    S.xbars = S.cbars + 32;
-    S.wait = WaitCtx{p.status, reinterpret_cast<volatile int*>(S.gbase + S.L.bars + 8 * (2 * S.L.nslot + 2 * S.L.nss + 10))};
+    S.bars = Bars{S.base + S.L.bars, S.L.nslot, S.L.nss, S.L.nrb, S.base + S.L.tags};
+    S.wait = WaitCtx{p.status, reinterpret_cast<volatile int*>(S.gbase + (S.bars.abort_flag() - S.base))};
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -630,25 +748,35 @@ __global__ void __launch_bounds__(Roles<P>::kThreads, 1)
     pl.kblk0 = pl.kb0 * 8;
     pl.kblk1 = min(p.nblk, pl.kb1 * 8);
 
-    if (threadIdx.x == 0) {
+    if (warp == 0) {
+        // Warp 0 initialises the barriers and tags, one lane per ring / scale
+        // slot; each lane fences its own inits.
         const Bars& bars = S.bars;
-        for (uint32_t s = 0; s < S.L.nslot; ++s) {
+        // Warps that own chunks of a unit: the arrivals its reduction buffer
+        // and scale slot wait for (at least 1 so the count is valid; a rank
+        // with no K steps has no owners and never waits on them).
+        const int cpu = (pl.kb1 - pl.kb0) / static_cast<int>(S.L.group);
+        const uint32_t nown = static_cast<uint32_t>(max(1, min(cpu, P::NCW)));
+        for (uint32_t s = lane; s < S.L.nslot; s += 32) {
             mbar_init(bars.full(s), 1);
-            mbar_init(bars.empty(s), S.L.steps);  // one arrival per K step of the stage
+            mbar_init(bars.empty(s), S.L.steps / S.L.group);  // one arrival per consumer chunk of the stage
+            sts_u32_volatile(bars.ring_tag(s), 0xffffffffu);
         }
-        for (uint32_t s = 0; s < S.L.nss; ++s) {
+        for (uint32_t s = lane; s < S.L.nss; s += 32) {
             mbar_init(bars.sfull(s), 1);
-            mbar_init(bars.sempty(s), P::NCW);
+            mbar_init(bars.sempty(s), nown);
+            sts_u32_volatile(bars.scale_tag(s), 0xffffffffu);
         }
-        for (uint32_t b = 0; b < 2; ++b) {
-            mbar_init(bars.rfull(b), P::NCW);
-            mbar_init(bars.rempty(b), 1);
-            mbar_init(S.cbars + 8 * b, pl.cl > 1 ? 32 * (pl.cl - 1) : 1);  // cfull
-            mbar_init(S.cbars + 16 + 8 * b, 32);                          // cempty
-            mbar_init(S.xbars + 8 * b, P::NCW);                            // staging
+        if (lane < S.L.nrb) mbar_init(bars.rfull(lane), nown);
+        if (lane < 2) {
+            mbar_init(bars.cfull(lane), pl.cl > 1 ? pl.cl - 1 : 1);  // one arrival per other rank
+            mbar_init(bars.cempty(lane), 1);                        // the leader's "slot free"
+            mbar_init(bars.xbar(lane), P::NCW);                     // staging
         }
-        *S.wait.abort = 0;
-        fence_barrier_init();
+        if (lane == 2) mbar_init(bars.xbar(2), 1);
+        if (lane == 3) sts_u32_volatile(bars.progress(), 0);
+        if (lane == 4) *S.wait.abort = 0;
+        fence_barrier_init();  // visible to the bulk-copy (async) proxy and to cluster peers
     }
     if (pl.cl > 1)
         cluster_sync_all();

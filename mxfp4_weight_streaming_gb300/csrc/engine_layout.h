@@ -10,6 +10,8 @@ struct SmemLayout {
     uint32_t ring;      // weight ring: nslot stages of steps x BOXES x 2048 bytes
     uint32_t nslot;
     uint32_t steps;     // K steps (256 values) per stage; divides every CTA's steps per unit
+    uint32_t group;     // K steps a consumer warp takes at a time (divides steps)
+    uint32_t nred;      // partial-sum slots per unit: min(chunks of `group` steps per unit, consumer warps)
     uint32_t xs;        // staged activations, f16 [xcols][blocks][32], column stride xs_stride
     uint32_t fx;        // activation block factors, f32 [4*NT column pairs][blocks][2], stride fx_stride
     uint32_t xs_stride; // bytes per staged column (blocks*64 + 16: the pad spreads columns over banks)
@@ -17,17 +19,20 @@ struct SmemLayout {
     uint32_t sc;        // scale ring: nss slots of ss_bytes
     uint32_t nss;
     uint32_t ss_bytes;  // one unit's scales: BOXES x 16 x K/32 bytes
-    uint32_t red;       // double-buffered reduction area (per consumer warp)
+    uint32_t red;       // reduction area: nrb unit buffers x nred partial slots
+    uint32_t nrb;       // units whose partials may be in flight to the reducer
     uint32_t fin;       // double-buffered per-unit sums of this CTA
     uint32_t recv;      // cluster leader: the other ranks' sums, [2][cl-1]
-    uint32_t bars;      // mbarriers (ring, scales, reduction, cluster)
+    uint32_t bars;      // mbarriers: full/empty[nslot], sfull/sempty[nss], rfull[nrb], cluster[4], staging[3], abort
+    uint32_t tags;      // u32 words: stage last issued into each ring slot [nslot], unit last
+                        // issued into each scale slot [nss], units the reducer has finished
     uint32_t total;
 };
 
-// K steps per stage: the largest count <= 8 / boxes that divides every
-// CTA's steps per unit (steps_a and steps_b; 0 counts as divisible).
-inline int stage_steps(int boxes, int steps_a, int steps_b) {
-    for (int s = 8 / boxes; s > 1; --s)
+// K steps per stage: the largest count <= max_steps / boxes that divides
+// every CTA's steps per unit (steps_a and steps_b; 0 counts as divisible).
+inline int stage_steps(int boxes, int steps_a, int steps_b, int max_steps = 8) {
+    for (int s = max_steps / boxes; s > 1; --s)
         if (steps_a % s == 0 && steps_b % s == 0) return s;
     return 1;
 }
@@ -36,9 +41,12 @@ inline int stage_steps(int boxes, int steps_a, int steps_b) {
 // the staged activations; the scale ring is deep enough that the producer is
 // never held back by it. Returns false if nothing fits.
 // nblk is the number of 32-blocks this CTA stages (its part of K); nblk_all
-// is the whole row's count (scales cover all of K); steps is the stage size.
+// is the whole row's count (scales cover all of K); steps is the stage size
+// and group the consumer chunk (a divisor of steps); unit_steps is the
+// largest number of K steps a CTA streams per unit.
 inline bool plan_layout(int nt, int boxes, int nblk, int nblk_all, int xcols, int cl, int consumer_warps,
-                        int red_stride, int steps, int max_smem, SmemLayout* out) {
+                        int red_stride, int steps, int group, int unit_steps, int max_smem, SmemLayout* out) {
+    if (group < 1 || steps % group != 0) return false;
     auto al = [](uint32_t v, uint32_t a) { return (v + a - 1) / a * a; };
     const int nkb = (nblk + 7) / 8;
     const uint32_t slot_bytes = 2048u * boxes * steps;
@@ -47,42 +55,55 @@ inline bool plan_layout(int nt, int boxes, int nblk, int nblk_all, int xcols, in
     const uint32_t xs_bytes = static_cast<uint32_t>(xcols) * xs_stride;
     const uint32_t fx_bytes = static_cast<uint32_t>(4 * nt) * fx_stride;
     const uint32_t ss_bytes = al(static_cast<uint32_t>(boxes) * 16 * nblk_all, 16);
-    const uint32_t red_bytes = 2u * consumer_warps * boxes * 8 * nt * red_stride * 4;
+    int nred = (unit_steps + group - 1) / group;
+    nred = nred < 1 ? 1 : (nred > consumer_warps ? consumer_warps : nred);
+    const uint32_t red_unit_bytes = static_cast<uint32_t>(nred) * boxes * 8 * nt * red_stride * 4;
     const uint32_t fin_bytes = 2u * boxes * 8 * nt * 16 * 4;
     const uint32_t recv_bytes = cl > 1 ? fin_bytes * (cl - 1) : 0;
     const int budget = max_smem - 1024;
     const int max_slots = static_cast<int>((128u * 1024u) / slot_bytes) < 2 ? 2 : static_cast<int>((128u * 1024u) / slot_bytes);
-    for (int nslot = max_slots; nslot >= 2; --nslot) {
-        int nss = (nslot * steps + nkb - 1) / (nkb > 0 ? nkb : 1) + 1;
-        nss = nss < 2 ? 2 : (nss > 16 ? 16 : nss);
-        SmemLayout l{};
-        uint32_t off = 0;
-        l.ring = off;
-        l.nslot = nslot;
-        l.steps = steps;
-        off += nslot * slot_bytes;
-        l.xs = off;
-        l.xs_stride = xs_stride;
-        off += xs_bytes;
-        l.fx = off;
-        l.fx_stride = fx_stride;
-        off += fx_bytes;
-        l.sc = off;
-        l.nss = nss;
-        l.ss_bytes = ss_bytes;
-        off += nss * ss_bytes;
-        l.red = off;
-        off += red_bytes;
-        l.fin = off;
-        off += fin_bytes;
-        l.recv = off;
-        off += recv_bytes;
-        l.bars = al(off, 8);
-        off = l.bars + 8 * (2 * nslot + 2 * nss + 4 + 4 + 2) + 8;  // + staging barriers + abort flag
-        l.total = off;
-        if (static_cast<int>(off) <= budget) {
-            *out = l;
-            return true;
+    // Prefer 4 reduction buffers (owners of 4 consecutive units can hand in
+    // their partials without waiting) while the ring keeps >= 4 slots.
+    for (int pass = 0; pass < 2; ++pass) {
+        const int nrb = pass == 0 ? 4 : 2;
+        const uint32_t red_bytes = static_cast<uint32_t>(nrb) * red_unit_bytes;
+        for (int nslot = max_slots; nslot >= (pass == 0 ? 4 : 2); --nslot) {
+            int nss = (nslot * steps + nkb - 1) / (nkb > 0 ? nkb : 1) + 1;
+            nss = nss < 2 ? 2 : (nss > 16 ? 16 : nss);
+            SmemLayout l{};
+            uint32_t off = 0;
+            l.ring = off;
+            l.nslot = nslot;
+            l.steps = steps;
+            l.group = group;
+            l.nred = nred;
+            off += nslot * slot_bytes;
+            l.xs = off;
+            l.xs_stride = xs_stride;
+            off += xs_bytes;
+            l.fx = off;
+            l.fx_stride = fx_stride;
+            off += fx_bytes;
+            l.sc = off;
+            l.nss = nss;
+            l.ss_bytes = ss_bytes;
+            off += nss * ss_bytes;
+            l.red = off;
+            l.nrb = nrb;
+            off += red_bytes;
+            l.fin = off;
+            off += fin_bytes;
+            l.recv = off;
+            off += recv_bytes;
+            l.bars = al(off, 8);
+            off = l.bars + 8 * (2 * nslot + 2 * nss + nrb + 4 + 3 + 1);
+            l.tags = off;
+            off += 4 * (nslot + nss + 1);
+            l.total = off;
+            if (static_cast<int>(off) <= budget) {
+                *out = l;
+                return true;
+            }
         }
     }
     return false;

@@ -23,7 +23,7 @@ struct DenseProblem {
     static constexpr int BOXES = 1;
     // More consumer warps hide more latency; fewer leave more registers for
     // the wider token tiles.
-    static constexpr int NCW = NT == 1 ? 16 : (NT == 2 ? 12 : 8);
+    static constexpr int NCW = NT == 1 ? 14 : (NT == 2 ? 12 : 8);
     using Params = LinearParams;
 
     __device__ static int num_units(const Params& p) { return p.n_rg; }
@@ -35,33 +35,11 @@ struct DenseProblem {
     __device__ static int unit_rows(const Params& p, int u) { return min(16, p.N - u * 16); }
     __device__ static int ncols(const Params& p, int) { return p.T; }
 
-    __device__ static void stage(const Params& p, int, int kblk0, int kblk1, const StageDst& dst, int tid,
-                                 int nthreads) {
-        const int T = p.T;
-        const int nb = kblk1 - kblk0;
-        // Items (block b, token t) = tid, tid + nthreads, ...; (b, t) advance
-        // without a division per item.
-        const int db = nthreads / T, dt = nthreads - (nthreads / T) * T;
-        int b = tid / T, t = tid - (tid / T) * T;
-        for (; b < nb; b += db, t += dt) {
-            if (t >= T) {
-                t -= T;
-                ++b;
-                if (b >= nb) break;
-            }
-            const uint4* src = reinterpret_cast<const uint4*>(p.x + (size_t)t * p.K + (size_t)(kblk0 + b) * 32);
-            uint4 v[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) v[q] = __ldg(src + q);
-            const uint32_t w[16] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w,
-                                    v[2].x, v[2].y, v[2].z, v[2].w, v[3].x, v[3].y, v[3].z, v[3].w};
-            stage_bf16_block(w, dst.col(t, b), dst.factor(t, b));
-        }
-        // Factors of the unused columns of the 8*NT-wide tiles are zero.
-        for (int it = tid; it < nb * (8 * NT - T); it += nthreads) {
-            const int b = it / (8 * NT - T);
-            *dst.factor(T + (it - b * (8 * NT - T)), b) = 0.0f;
-        }
+    // Staged columns are the T token rows of x (bf16), copied in bulk.
+    static constexpr bool kBulkStage = true;
+    __device__ static int stage_cols(const Params& p, int) { return p.T; }
+    __device__ static const uint8_t* stage_row(const Params& p, int, int col) {
+        return reinterpret_cast<const uint8_t*>(p.x + static_cast<size_t>(col) * p.K);
     }
 
     __device__ static void epilogue(const Params& p, int u, const Sums<NT>& v, int lane) {
@@ -101,7 +79,7 @@ bool plan_linear(int T, int K, int max_smem, int* cl, SmemLayout* L) {
             g = a;
         }
         const int steps = stage_steps(1, g, 0);
-        if (plan_layout(nt, 1, nb_local, nblk, T, c, ncw, kRedStride, steps, max_smem, L)) {
+        if (plan_layout(nt, 1, nb_local, nblk, T, c, ncw, kRedStride, steps, steps, nkb_c, max_smem, L)) {
             *cl = c;
             return true;
         }

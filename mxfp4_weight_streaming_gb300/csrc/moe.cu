@@ -262,29 +262,12 @@ struct GateUpProblem {
     __device__ static int unit_rows(const Params&, int) { return 16; }
     __device__ static int ncols(const Params& p, int q) { return p.w.c1_cnt[q]; }
 
-    __device__ static void stage(const Params& p, int q, int kblk0, int kblk1, const StageDst& dst, int tid,
-                                 int nthreads) {
-        const int cnt = p.w.c1_cnt[q];
-        const int start = p.w.c1_start[q];
-        const int nb = kblk1 - kblk0;
-        const int items = nb * cnt;
-        for (int it = tid; it < items; it += nthreads) {
-            const int b = it / cnt;
-            const int t = it - b * cnt;
-            const int token = p.w.sorted[start + t] / p.top_k;
-            const uint4* src =
-                reinterpret_cast<const uint4*>(p.x + (size_t)token * p.hidden + (size_t)(kblk0 + b) * 32);
-            uint4 v[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) v[k] = __ldg(src + k);
-            const uint32_t wv[16] = {v[0].x, v[0].y, v[0].z, v[0].w, v[1].x, v[1].y, v[1].z, v[1].w,
-                                     v[2].x, v[2].y, v[2].z, v[2].w, v[3].x, v[3].y, v[3].z, v[3].w};
-            stage_bf16_block(wv, dst.col(t, b), dst.factor(t, b));
-        }
-        for (int it = tid; it < nb * (8 - cnt); it += nthreads) {
-            const int b = it / (8 - cnt);
-            *dst.factor(cnt + (it - b * (8 - cnt)), b) = 0.0f;
-        }
+    // Staged columns are the chunk's token rows of x (bf16), copied in bulk.
+    static constexpr bool kBulkStage = true;
+    __device__ static int stage_cols(const Params& p, int q) { return p.w.c1_cnt[q]; }
+    __device__ static const uint8_t* stage_row(const Params& p, int q, int col) {
+        const int token = p.w.sorted[p.w.c1_start[q] + col] / p.top_k;
+        return reinterpret_cast<const uint8_t*>(p.x + static_cast<size_t>(token) * p.hidden);
     }
 
     __device__ static void epilogue(const Params& p, int u, const Sums<1>& v, int lane) {
@@ -333,7 +316,9 @@ struct DownProblem {
     __device__ static int unit_rows(const Params&, int) { return 16; }
     __device__ static int ncols(const Params& p, int q) { return 2 * p.w.c2_cnt[q]; }
 
-    // Column t holds hi(h_t), column cnt + t holds lo(h_t).
+    // Column t holds hi(h_t), column cnt + t holds lo(h_t); staged by the
+    // consumer threads from the fp32 rows of h.
+    static constexpr bool kBulkStage = false;
     __device__ static void stage(const Params& p, int q, int kblk0, int kblk1, const StageDst& dst, int tid,
                                  int nthreads) {
         const int cnt = p.w.c2_cnt[q];
@@ -409,7 +394,11 @@ int launch_moe(const uint8_t* w1q, const uint8_t* w2q, const MoeArgs& a, int num
     g.xcols = kChunkGateUp;
     g.upc = a.inter / 16;
     g.cl = 1;
-    if (!plan_layout(1, 2, g.nblk, g.nblk, g.xcols, 1, GateUpProblem::NCW, kRedStride, stage_steps(2, g.nkb, 0),
+    // Consumer chunks of half a stage keep every consumer warp supplied from
+    // the ring (8 stages of 16 KB hold 16 chunks for 12 warps).
+    const int steps1 = stage_steps(2, g.nkb, 0);
+    const int group1 = steps1 % 2 == 0 ? steps1 / 2 : steps1;
+    if (!plan_layout(1, 2, g.nblk, g.nblk, g.xcols, 1, GateUpProblem::NCW, kRedStride, steps1, group1, g.nkb,
                      max_smem, &g.layout))
         return MXFP4_ERR_SHAPE;
 
@@ -424,7 +413,9 @@ int launch_moe(const uint8_t* w1q, const uint8_t* w2q, const MoeArgs& a, int num
     d.xcols = 2 * kChunkDown;
     d.upc = a.hidden / 16;
     d.cl = 1;
-    if (!plan_layout(1, 1, d.nblk, d.nblk, d.xcols, 1, DownProblem::NCW, kRedStride, stage_steps(1, d.nkb, 0),
+    const int steps2 = stage_steps(1, d.nkb, 0);
+    const int group2 = steps2 % 2 == 0 ? steps2 / 2 : steps2;
+    if (!plan_layout(1, 1, d.nblk, d.nblk, d.xcols, 1, DownProblem::NCW, kRedStride, steps2, group2, d.nkb,
                      max_smem, &d.layout))
         return MXFP4_ERR_SHAPE;
 

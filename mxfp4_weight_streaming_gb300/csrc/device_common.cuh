@@ -44,18 +44,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
-// Nanoseconds a waiting thread may be suspended inside one try_wait (it is
-// woken when the phase completes); keeps idle warps from spinning on issue
-// slots the working warps need.
-constexpr uint32_t kSuspendHintNs = 20000;
-
+// One potentially blocking test of the phase (the hardware's own time
+// limit applies; a suspend-time hint measured no better).
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity), "n"(kSuspendHintNs)
+        : "r"(bar), "r"(parity)
         : "memory");
     return ok != 0;
 }
@@ -118,6 +115,12 @@ __device__ __forceinline__ bool wait_shared_value(uint32_t addr, uint32_t want, 
             return false;
         }
     }
+}
+
+__device__ __forceinline__ uint32_t atom_add_shared(uint32_t a, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.shared.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(a), "r"(v) : "memory");
+    return old;
 }
 
 // Waits until the shared counter at addr is >= want.

@@ -69,6 +69,10 @@ struct Bars {
     __device__ uint32_t ring_tag(uint32_t s) const { return tags + 4 * s; }
     __device__ uint32_t scale_tag(uint32_t s) const { return tags + 4 * (nslot + s); }
     __device__ uint32_t progress() const { return tags + 4 * (nslot + nss); }
+    // Per reduction buffer (lone CTAs): unit whose partials it last held,
+    // and how many owners have handed in theirs.
+    __device__ uint32_t red_tag(uint32_t b) const { return tags + 4 * (nslot + nss + 1 + b); }
+    __device__ uint32_t red_count(uint32_t b) const { return tags + 4 * (nslot + nss + 1 + nrb + b); }
 };
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx& w) {
@@ -358,9 +362,20 @@ __device__ __forceinline__ void consume_step_full(uint32_t slot, uint32_t box_st
 
 // Final per-unit sums handed to a problem's epilogue: [box][column][16 rows].
 template <int NT>
+// A unit's sum for (box, col, row) is the sum, in order, of nparts partial
+// arrays part_stride floats apart, each [box][column][row] with row_stride
+// floats per column.
 struct Sums {
     const float* f;
-    __device__ float sum(int box, int col, int r) const { return f[(box * 8 * NT + col) * 16 + r]; }
+    int nparts;
+    int part_stride;
+    int row_stride;
+    __device__ float sum(int box, int col, int r) const {
+        const float* q = f + (box * 8 * NT + col) * row_stride + r;
+        float s = 0.f;
+        for (int j = 0; j < nparts; ++j) s += q[j * part_stride];
+        return s;
+    }
 };
 
 // Where a CTA sits: which units, which part of K.
@@ -498,6 +513,7 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
     // which sits in ring slot stage % nslot.
     const uint32_t cps = spb / G;
     const uint32_t cpu = static_cast<uint32_t>(nkbc) / G;
+    const uint32_t nown = cpu < static_cast<uint32_t>(P::NCW) ? cpu : static_cast<uint32_t>(P::NCW);
     const uint32_t ring = S.base + L.ring;
     const uint32_t box_stride = spb * kBoxBytes;
     const uint32_t adv_stage = P::NCW / cps, adv_within = P::NCW - (P::NCW / cps) * cps;
@@ -586,11 +602,17 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
                 }
             }
         }
-        // Reduction buffer uu % nrb is free once the reducer has finished
-        // unit uu - nrb.
+        // Reduction buffer uu % nrb is free once unit uu - nrb is finished:
+        // by the reducer (clusters), else by that unit's last owner, which
+        // tags the buffer with its unit.
         const uint32_t rb = uu % L.nrb;
-        if (!__all_sync(0xffffffffu, wait_shared_at_least(bars.progress(), uu + 1 - min(uu + 1, L.nrb), S.wait)))
+        const bool lone = pl.cl == 1;
+        if (lone) {
+            if (!__all_sync(0xffffffffu, wait_shared_value(bars.red_tag(rb), uu - L.nrb, S.wait))) return;
+        } else if (!__all_sync(0xffffffffu,
+                               wait_shared_at_least(bars.progress(), uu + 1 - min(uu + 1, L.nrb), S.wait))) {
             return;
+        }
         {
             float* R = redw + (rb * L.nred + jred) * kRedWarpFloats;
             const int g = lane >> 2, tig = lane & 3;
@@ -607,7 +629,30 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
                 }
         }
         __syncwarp();
-        if (lane == 0) {
+        if (lone) {
+            // The owner that hands in the last partial sums them (in K order,
+            // the same order the reducer uses) and runs the epilogue, so the
+            // per-unit work is spread over the consumer warps.
+            uint32_t prev = 0;
+            if (lane == 0) {
+                __threadfence_block();
+                prev = atom_add_shared(bars.red_count(rb), 1u);
+            }
+            prev = __shfl_sync(0xffffffffu, prev, 0);
+            if (prev + 1 == nown) {
+                __threadfence_block();
+                P::epilogue(p, u, Sums<NT>{redw + rb * L.nred * kRedWarpFloats, static_cast<int>(nown), kRedWarpFloats,
+                                           kRedStride},
+                            lane);
+                __syncwarp();
+                if (lane == 0) {
+                    sts_u32_volatile(bars.red_count(rb), 0);
+                    __threadfence_block();
+                    sts_u32_volatile(bars.red_tag(rb), uu);
+                }
+            }
+            if (lane == 0) mbar_arrive(bars.sempty(ss));
+        } else if (lane == 0) {
             mbar_arrive(bars.rfull(rb));
             mbar_arrive(bars.sempty(ss));
         }
@@ -625,6 +670,7 @@ __device__ void reducer_role(const typename P::Params& p, const Smem& S, const P
     const float* red = reinterpret_cast<const float*>(S.gbase + L.red);
     float* fin = reinterpret_cast<float*>(S.gbase + L.fin);
     const float* recv = reinterpret_cast<const float*>(S.gbase + L.recv);
+    if (pl.cl == 1) return;  // lone CTAs: each unit's last owner finishes it
     // Partials per unit: one per consumer warp that owns chunks of it.
     const int cpu = (pl.kb1 - pl.kb0) / static_cast<int>(L.group);
     const int nown = cpu < P::NCW ? cpu : P::NCW;
@@ -693,10 +739,11 @@ __device__ void reducer_role(const typename P::Params& p, const Smem& S, const P
             __syncwarp();
             // The other ranks may refill slot rb: every lane's reads of it
             // are done (their values are in F).
-            if (lane == 0)
-                for (uint32_t q = 1; q < pl.cl; ++q) mbar_arrive_remote_relaxed(map_to_rank(bars.cempty(rb), q));
+            // Lane q signals rank q (the remote arrives go out in parallel).
+            if (lane >= 1 && static_cast<uint32_t>(lane) < pl.cl)
+                mbar_arrive_remote_relaxed(map_to_rank(bars.cempty(rb), static_cast<uint32_t>(lane)));
         }
-        P::epilogue(p, u, Sums<NT>{F}, lane);
+        P::epilogue(p, u, Sums<NT>{F, 1, 0, 16}, lane);
         __syncwarp();
     }
 }
@@ -767,7 +814,11 @@ __global__ void __launch_bounds__(Roles<P>::kThreads, 1)
             mbar_init(bars.sempty(s), nown);
             sts_u32_volatile(bars.scale_tag(s), 0xffffffffu);
         }
-        if (lane < S.L.nrb) mbar_init(bars.rfull(lane), nown);
+        if (lane < S.L.nrb) {
+            mbar_init(bars.rfull(lane), nown);
+            sts_u32_volatile(bars.red_tag(lane), lane - S.L.nrb);  // "unit lane - nrb" released it
+            sts_u32_volatile(bars.red_count(lane), 0);
+        }
         if (lane < 2) {
             mbar_init(bars.cfull(lane), pl.cl > 1 ? pl.cl - 1 : 1);  // one arrival per other rank
             mbar_init(bars.cempty(lane), 1);                        // the leader's "slot free"

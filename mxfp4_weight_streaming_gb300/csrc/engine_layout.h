@@ -25,7 +25,8 @@ struct SmemLayout {
     uint32_t recv;      // cluster leader: the other ranks' sums, [2][cl-1]
     uint32_t bars;      // mbarriers: full/empty[nslot], sfull/sempty[nss], rfull[nrb], cluster[4], staging[3], abort
     uint32_t tags;      // u32 words: stage last issued into each ring slot [nslot], unit last
-                        // issued into each scale slot [nss], units the reducer has finished
+                        // issued into each scale slot [nss], units the reducer has finished,
+                        // per reduction buffer: unit last finished [nrb], partials handed in [nrb]
     uint32_t total;
 };
 
@@ -98,7 +99,7 @@ inline bool plan_layout(int nt, int boxes, int nblk, int nblk_all, int xcols, in
             l.bars = al(off, 8);
             off = l.bars + 8 * (2 * nslot + 2 * nss + nrb + 4 + 3 + 1);
             l.tags = off;
-            off += 4 * (nslot + nss + 1);
+            off += 4 * (nslot + nss + 1 + 2 * nrb);
             l.total = off;
             if (static_cast<int>(off) <= budget) {
                 *out = l;

@@ -8,19 +8,21 @@
 // with the same activation columns form a "chunk"; the activations of a
 // chunk are staged once into shared memory.
 //
-// One persistent CTA per SM, warp-specialised:
+// One persistent CTA per SM (or per cluster rank), warp-specialised:
 //   producer warp : per unit, one bulk copy of the scale bytes of each row
 //                   group (16 rows x K/32 contiguous bytes) into a scale
-//                   ring; per 256-wide K step, BOXES 2D TMA loads of
-//                   16 rows x 128 bytes (SWIZZLE_128B) into one ring slot.
-//   consumer warps: K steps are dealt round-robin over the warps. Per
-//                   32-value block: ldmatrix -> hardware E2M1 -> f16 unpack
-//                   -> two m16n8k16 MMAs (fp32 accumulate) per 8-column
-//                   tile -> partial * 2^(s-127) * column factor into fp32
-//                   accumulators. Per unit, each warp writes its partials
-//                   to a double-buffered reduction area.
-//   reducer warp  : sums the warps' partials in a fixed order and runs the
-//                   problem's epilogue (deterministic, no atomics).
+//                   ring; per stage (spb K steps of 256 values), one TMA
+//                   copy per box of 16 rows x spb 128-byte segments
+//                   (SWIZZLE_128B) into a ring slot, which it tags with the
+//                   stage index.
+//   consumer warps: the K steps are cut into chunks of G steps, dealt
+//                   round-robin over the warps. Per 32-value block: ldmatrix
+//                   -> hardware E2M1 -> f16 unpack -> two m16n8k16 MMAs
+//                   (fp32 accumulate) per 8-column tile -> partial scaled by
+//                   2^(s-127) * column factor (f32x2) into the accumulators.
+//                   Per unit, each owning warp hands its partial to a
+//                   reduction buffer; one owner sums the partials in a fixed
+//                   order and runs the problem's epilogue (deterministic).
 // Every wait is bounded (see device_common.cuh); on a timeout the kernel
 // records it in the status word and winds down.
 #pragma once
@@ -35,13 +37,12 @@
 
 namespace mxfp4 {
 
-// Warps of a CTA: P::NCW consumers, then the reducer, then the producer.
+// Warps of a CTA: P::NCW consumers, then the producer.
 template <class P>
 struct Roles {
     static constexpr int kConsumers = P::NCW;
-    static constexpr int kReducer = P::NCW;
-    static constexpr int kProducer = P::NCW + 1;
-    static constexpr int kThreads = (P::NCW + 2) * 32;
+    static constexpr int kProducer = P::NCW;
+    static constexpr int kThreads = (P::NCW + 1) * 32;
     static constexpr int kConsumerThreads = P::NCW * 32;
 };
 constexpr int kBoxBytes = 2048;  // 16 rows x 128 bytes = 16 rows x 256 K values
@@ -57,22 +58,18 @@ struct Bars {
     __device__ uint32_t empty(uint32_t s) const { return base + 8 * (nslot + s); }
     __device__ uint32_t sfull(uint32_t s) const { return base + 8 * (2 * nslot + s); }
     __device__ uint32_t sempty(uint32_t s) const { return base + 8 * (2 * nslot + nss + s); }
-    __device__ uint32_t rfull(uint32_t b) const { return base + 8 * (2 * nslot + 2 * nss + b); }
-    __device__ uint32_t cfull(uint32_t b) const { return base + 8 * (2 * nslot + 2 * nss + nrb + b); }
-    __device__ uint32_t cempty(uint32_t b) const { return base + 8 * (2 * nslot + 2 * nss + nrb + 2 + b); }
     // xbar(0), xbar(1): all consumers before / after staging; xbar(2): the
     // bulk copies of raw activations have landed.
-    __device__ uint32_t xbar(uint32_t b) const { return base + 8 * (2 * nslot + 2 * nss + nrb + 4 + b); }
-    __device__ uint32_t abort_flag() const { return base + 8 * (2 * nslot + 2 * nss + nrb + 7); }
-    // Stage last issued into ring slot s; unit last issued into scale slot s;
-    // number of units the reducer has finished reading.
+    __device__ uint32_t xbar(uint32_t b) const { return base + 8 * (2 * nslot + 2 * nss + b); }
+    __device__ uint32_t abort_flag() const { return base + 8 * (2 * nslot + 2 * nss + 3); }
+    // Stage last issued into ring slot s; unit last issued into scale slot s.
     __device__ uint32_t ring_tag(uint32_t s) const { return tags + 4 * s; }
     __device__ uint32_t scale_tag(uint32_t s) const { return tags + 4 * (nslot + s); }
-    __device__ uint32_t progress() const { return tags + 4 * (nslot + nss); }
-    // Per reduction buffer (lone CTAs): unit whose partials it last held,
-    // and how many owners have handed in theirs.
-    __device__ uint32_t red_tag(uint32_t b) const { return tags + 4 * (nslot + nss + 1 + b); }
-    __device__ uint32_t red_count(uint32_t b) const { return tags + 4 * (nslot + nss + 1 + nrb + b); }
+    // Per reduction buffer: unit whose partials it last held (a copy on
+    // every cluster rank), and how many owners have handed in theirs (the
+    // count on rank 0 is the one used).
+    __device__ uint32_t red_tag(uint32_t b) const { return tags + 4 * (nslot + nss + b); }
+    __device__ uint32_t red_count(uint32_t b) const { return tags + 4 * (nslot + nss + nrb + b); }
 };
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx& w) {
@@ -487,6 +484,15 @@ __device__ void producer_role(const typename P::Params& p, const Smem& S, const 
     }
 }
 
+// Consumer warps that own chunks of each unit on cluster rank q (the same
+// split of K steps the placement uses).
+__device__ __forceinline__ int rank_owners(int nkb, int cl, int q, int group, int ncw) {
+    const int nkb_c = (nkb + cl - 1) / cl;
+    const int k0 = min(nkb, q * nkb_c);
+    const int k1 = min(nkb, k0 + nkb_c);
+    return min((k1 - k0) / group, ncw);
+}
+
 template <class P>
 __device__ void consumer_role(const typename P::Params& p, const Smem& S, const Placement& pl, int warp, int lane) {
     constexpr int NT = P::NT;
@@ -513,7 +519,18 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
     // which sits in ring slot stage % nslot.
     const uint32_t cps = spb / G;
     const uint32_t cpu = static_cast<uint32_t>(nkbc) / G;
-    const uint32_t nown = cpu < static_cast<uint32_t>(P::NCW) ? cpu : static_cast<uint32_t>(P::NCW);
+    // Partial slots of a unit: rank q's owners use [base_q, base_q + owners_q)
+    // of the buffer on rank 0; `total` counts every rank's owners.
+    const int ranks = static_cast<int>(pl.cl);
+    uint32_t rbase = 0, total = 0;
+    for (int q = 0; q < ranks; ++q) {
+        const uint32_t o = static_cast<uint32_t>(rank_owners(p.nkb, ranks, q, static_cast<int>(G), P::NCW));
+        if (q < static_cast<int>(pl.rank)) rbase += o;
+        total += o;
+    }
+    const bool lone = pl.cl == 1;
+    const uint32_t red0 = lone ? S.base + L.red : map_to_rank(S.base + L.red, 0);  // rank 0's buffers
+    const uint32_t count0 = lone ? 0u : map_to_rank(bars.red_count(0), 0);
     const uint32_t ring = S.base + L.ring;
     const uint32_t box_stride = spb * kBoxBytes;
     const uint32_t adv_stage = P::NCW / cps, adv_within = P::NCW - (P::NCW / cps) * cps;
@@ -554,7 +571,7 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
         // its partial goes to slot c - cb (< NCW, since its previous chunk
         // lies before the unit).
         // Only owners take part in the unit: they wait for its scales, hand
-        // their partial to the reducer and release the scale slot.
+        // in their partial and release the scale slot.
         if (c >= cb + cpu) continue;
         const uint32_t jred = c - cb;
         uint64_t acc[BOXES][NT][2];
@@ -602,149 +619,80 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
                 }
             }
         }
-        // Reduction buffer uu % nrb is free once unit uu - nrb is finished:
-        // by the reducer (clusters), else by that unit's last owner, which
-        // tags the buffer with its unit.
+        // Reduction buffer uu % nrb (on rank 0) is free once unit uu - nrb is
+        // finished; its finisher tags the buffer on every rank.
         const uint32_t rb = uu % L.nrb;
-        const bool lone = pl.cl == 1;
-        if (lone) {
-            if (!__all_sync(0xffffffffu, wait_shared_value(bars.red_tag(rb), uu - L.nrb, S.wait))) return;
-        } else if (!__all_sync(0xffffffffu,
-                               wait_shared_at_least(bars.progress(), uu + 1 - min(uu + 1, L.nrb), S.wait))) {
-            return;
-        }
+        if (!__all_sync(0xffffffffu, wait_shared_value(bars.red_tag(rb), uu - L.nrb, S.wait))) return;
+        if (lone)
+            __threadfence_block();
+        else
+            fence_acq_rel_cluster();
         {
-            float* R = redw + (rb * L.nred + jred) * kRedWarpFloats;
+            const uint32_t slot_f = (rb * L.nred_all + rbase + jred) * kRedWarpFloats;
             const int g = lane >> 2, tig = lane & 3;
 #pragma unroll
             for (int bx = 0; bx < BOXES; ++bx)
 #pragma unroll
                 for (int n = 0; n < NT; ++n) {
-                    float* Rb = R + (bx * 8 * NT + 8 * n + 2 * tig) * kRedStride;
+                    const uint32_t rb_f = slot_f + (bx * 8 * NT + 8 * n + 2 * tig) * kRedStride;
                     const float2 a01 = f32x2_unpack(acc[bx][n][0]), a23 = f32x2_unpack(acc[bx][n][1]);
-                    Rb[g] = a01.x;
-                    Rb[kRedStride + g] = a01.y;
-                    Rb[g + 8] = a23.x;
-                    Rb[kRedStride + g + 8] = a23.y;
+                    if (lone) {
+                        float* Rb = redw + rb_f;
+                        Rb[g] = a01.x;
+                        Rb[kRedStride + g] = a01.y;
+                        Rb[g + 8] = a23.x;
+                        Rb[kRedStride + g + 8] = a23.y;
+                    } else {
+                        st_cluster_f32(red0 + 4 * (rb_f + g), a01.x);
+                        st_cluster_f32(red0 + 4 * (rb_f + kRedStride + g), a01.y);
+                        st_cluster_f32(red0 + 4 * (rb_f + g + 8), a23.x);
+                        st_cluster_f32(red0 + 4 * (rb_f + kRedStride + g + 8), a23.y);
+                    }
                 }
         }
         __syncwarp();
-        if (lone) {
-            // The owner that hands in the last partial sums them (in K order,
-            // the same order the reducer uses) and runs the epilogue, so the
-            // per-unit work is spread over the consumer warps.
-            uint32_t prev = 0;
-            if (lane == 0) {
+        // Count the hand-in. Lone CTA: the owner that completes the count
+        // finishes the unit. Cluster: rank 0's first owner of the unit waits
+        // for every rank's partials and finishes it.
+        uint32_t prev = 0;
+        if (lane == 0) {
+            if (lone) {
                 __threadfence_block();
                 prev = atom_add_shared(bars.red_count(rb), 1u);
+            } else {
+                fence_acq_rel_cluster();
+                prev = atom_add_cluster(count0 + 4 * rb, 1u);
             }
-            prev = __shfl_sync(0xffffffffu, prev, 0);
-            if (prev + 1 == nown) {
+        }
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        bool finish = lone ? prev + 1 == total : (pl.rank == 0 && jred == 0);
+        if (finish && !lone) {
+            if (!__all_sync(0xffffffffu, wait_shared_value(bars.red_count(rb), total, S.wait))) return;
+        }
+        if (finish) {
+            if (lone)
                 __threadfence_block();
-                P::epilogue(p, u, Sums<NT>{redw + rb * L.nred * kRedWarpFloats, static_cast<int>(nown), kRedWarpFloats,
-                                           kRedStride},
-                            lane);
-                __syncwarp();
+            else
+                fence_acq_rel_cluster();
+            // Sum of the slots in order: rank 0's owners in K order, then
+            // rank 1's, ... (deterministic).
+            P::epilogue(p, u,
+                        Sums<NT>{redw + rb * L.nred_all * kRedWarpFloats, static_cast<int>(total), kRedWarpFloats,
+                                 kRedStride},
+                        lane);
+            __syncwarp();
+            if (lane == 0) sts_u32_volatile(bars.red_count(rb), 0);
+            if (lone) {
                 if (lane == 0) {
-                    sts_u32_volatile(bars.red_count(rb), 0);
                     __threadfence_block();
                     sts_u32_volatile(bars.red_tag(rb), uu);
                 }
+            } else {
+                fence_acq_rel_cluster();
+                if (lane < ranks) st_cluster_u32(map_to_rank(bars.red_tag(rb), static_cast<uint32_t>(lane)), uu);
             }
-            if (lane == 0) mbar_arrive(bars.sempty(ss));
-        } else if (lane == 0) {
-            mbar_arrive(bars.rfull(rb));
-            mbar_arrive(bars.sempty(ss));
         }
-    }
-}
-
-template <class P>
-__device__ void reducer_role(const typename P::Params& p, const Smem& S, const Placement& pl, int lane) {
-    constexpr int NT = P::NT;
-    constexpr int BOXES = P::BOXES;
-    constexpr int kRedWarpFloats = BOXES * 8 * NT * kRedStride;
-    constexpr int kFin = BOXES * 8 * NT * 16;  // floats of one unit's sums
-    const SmemLayout& L = S.L;
-    const Bars& bars = S.bars;
-    const float* red = reinterpret_cast<const float*>(S.gbase + L.red);
-    float* fin = reinterpret_cast<float*>(S.gbase + L.fin);
-    const float* recv = reinterpret_cast<const float*>(S.gbase + L.recv);
-    if (pl.cl == 1) return;  // lone CTAs: each unit's last owner finishes it
-    // Partials per unit: one per consumer warp that owns chunks of it.
-    const int cpu = (pl.kb1 - pl.kb0) / static_cast<int>(L.group);
-    const int nown = cpu < P::NCW ? cpu : P::NCW;
-    pdl_wait_previous();  // outputs may be read or written by the previous kernel
-    uint32_t b = 0, bphase = 0;  // reduction buffer uu % nrb and its phase
-    for (int u = pl.u0; u < pl.u1; ++u) {
-        const uint32_t uu = u - pl.u0;
-        const uint32_t rb = uu & 1;  // fin buffer and cluster slot
-        if (nown > 0 && !warp_wait(bars.rfull(b), bphase, S.wait)) return;
-        const int ncols = P::ncols(p, P::chunk_of(p, u));
-        // CTA-local sums over the unit's partials, in K order (slot j holds
-        // the chunks j, j + NCW, ... of the unit).
-        const float* R = red + b * L.nred * kRedWarpFloats;
-        float* F = fin + rb * kFin;
-#pragma unroll
-        for (int bx = 0; bx < BOXES; ++bx)
-            for (int e = lane; e < ncols * 16; e += 32) {
-                const int idx = bx * 8 * NT + (e >> 4), r = e & 15;
-                float s = 0.f;
-                for (int j = 0; j < nown; ++j) s += R[j * kRedWarpFloats + idx * kRedStride + r];
-                F[idx * 16 + r] = s;
-            }
-        // Buffer b may be refilled (by the owners of unit uu + nrb) once every
-        // lane's reads of it are done.
-        __syncwarp();
-        __threadfence_block();
-        if (lane == 0) sts_u32_volatile(bars.progress(), uu + 1);
-        if (++b == L.nrb) {
-            b = 0;
-            bphase ^= 1u;
-        }
-        if (pl.cl > 1) {
-            if (pl.rank != 0) {
-                // Send this CTA's part of K to the leader, in its rank's slot.
-                // One lane waits (cluster-scope acquire), the warp follows.
-                bool ok = true;
-                if (lane == 0) ok = mbar_wait_cluster(bars.cempty(rb), ((uu >> 1) & 1) ^ 1, S.wait);
-                if (!__shfl_sync(0xffffffffu, ok, 0)) return;
-                const uint32_t dst = map_to_rank(S.base + L.recv + ((rb * (pl.cl - 1) + pl.rank - 1) * kFin) * 4, 0);
-#pragma unroll
-                for (int bx = 0; bx < BOXES; ++bx)
-                    for (int e = lane; e < ncols * 16; e += 32) {
-                        const int idx = bx * 8 * NT * 16 + e;
-                        st_cluster_f32(dst + idx * 4, F[idx]);
-                    }
-                // All lanes' remote stores, then one cluster-scope release.
-                __syncwarp();
-                if (lane == 0) {
-                    fence_acq_rel_cluster();
-                    mbar_arrive_remote(map_to_rank(bars.cfull(rb), 0));
-                }
-                continue;
-            }
-            // Leader: add the other ranks' parts in rank order.
-            bool ok = true;
-            if (lane == 0) ok = mbar_wait_cluster(bars.cfull(rb), (uu >> 1) & 1, S.wait);
-            if (!__shfl_sync(0xffffffffu, ok, 0)) return;
-#pragma unroll
-            for (int bx = 0; bx < BOXES; ++bx)
-                for (int e = lane; e < ncols * 16; e += 32) {
-                    const int idx = bx * 8 * NT * 16 + e;
-                    float s = F[idx];
-                    for (uint32_t q = 0; q + 1 < pl.cl; ++q) s += recv[(rb * (pl.cl - 1) + q) * kFin + idx];
-                    F[idx] = s;
-                }
-            __syncwarp();
-            // The other ranks may refill slot rb: every lane's reads of it
-            // are done (their values are in F).
-            // Lane q signals rank q (the remote arrives go out in parallel).
-            if (lane >= 1 && static_cast<uint32_t>(lane) < pl.cl)
-                mbar_arrive_remote_relaxed(map_to_rank(bars.cempty(rb), static_cast<uint32_t>(lane)));
-        }
-        P::epilogue(p, u, Sums<NT>{F, 1, 0, 16}, lane);
-        __syncwarp();
+        if (lane == 0) mbar_arrive(bars.sempty(ss));
     }
 }
 
@@ -815,17 +763,11 @@ __global__ void __launch_bounds__(Roles<P>::kThreads, 1)
             sts_u32_volatile(bars.scale_tag(s), 0xffffffffu);
         }
         if (lane < S.L.nrb) {
-            mbar_init(bars.rfull(lane), nown);
             sts_u32_volatile(bars.red_tag(lane), lane - S.L.nrb);  // "unit lane - nrb" released it
             sts_u32_volatile(bars.red_count(lane), 0);
         }
-        if (lane < 2) {
-            mbar_init(bars.cfull(lane), pl.cl > 1 ? pl.cl - 1 : 1);  // one arrival per other rank
-            mbar_init(bars.cempty(lane), 1);                        // the leader's "slot free"
-            mbar_init(bars.xbar(lane), P::NCW);                     // staging
-        }
+        if (lane < 2) mbar_init(bars.xbar(lane), P::NCW);  // staging
         if (lane == 2) mbar_init(bars.xbar(2), 1);
-        if (lane == 3) sts_u32_volatile(bars.progress(), 0);
         if (lane == 4) *S.wait.abort = 0;
         fence_barrier_init();  // visible to the bulk-copy (async) proxy and to cluster peers
     }
@@ -840,8 +782,6 @@ __global__ void __launch_bounds__(Roles<P>::kThreads, 1)
 
     if (warp == Roles<P>::kProducer)
         producer_role<P>(p, S, pl, &tmap, lane);
-    else if (warp == Roles<P>::kReducer)
-        reducer_role<P>(p, S, pl, lane);
     else
         consumer_role<P>(p, S, pl, warp, lane);
 

@@ -19,14 +19,13 @@ struct SmemLayout {
     uint32_t sc;        // scale ring: nss slots of ss_bytes
     uint32_t nss;
     uint32_t ss_bytes;  // one unit's scales: BOXES x 16 x K/32 bytes
-    uint32_t red;       // reduction area: nrb unit buffers x nred partial slots
-    uint32_t nrb;       // units whose partials may be in flight to the reducer
-    uint32_t fin;       // double-buffered per-unit sums of this CTA
-    uint32_t recv;      // cluster leader: the other ranks' sums, [2][cl-1]
-    uint32_t bars;      // mbarriers: full/empty[nslot], sfull/sempty[nss], rfull[nrb], cluster[4], staging[3], abort
+    uint32_t red;       // reduction area: nrb unit buffers x nred_all partial slots (used on cluster rank 0)
+    uint32_t nrb;       // units whose partials may be in flight at once
+    uint32_t nred_all;  // partial slots per buffer: nred per cluster rank
+    uint32_t bars;      // mbarriers: full/empty[nslot], sfull/sempty[nss], staging[3], abort flag
     uint32_t tags;      // u32 words: stage last issued into each ring slot [nslot], unit last
-                        // issued into each scale slot [nss], units the reducer has finished,
-                        // per reduction buffer: unit last finished [nrb], partials handed in [nrb]
+                        // issued into each scale slot [nss], per reduction buffer: unit last
+                        // finished [nrb], partials handed in [nrb]
     uint32_t total;
 };
 
@@ -58,9 +57,8 @@ inline bool plan_layout(int nt, int boxes, int nblk, int nblk_all, int xcols, in
     const uint32_t ss_bytes = al(static_cast<uint32_t>(boxes) * 16 * nblk_all, 16);
     int nred = (unit_steps + group - 1) / group;
     nred = nred < 1 ? 1 : (nred > consumer_warps ? consumer_warps : nred);
-    const uint32_t red_unit_bytes = static_cast<uint32_t>(nred) * boxes * 8 * nt * red_stride * 4;
-    const uint32_t fin_bytes = 2u * boxes * 8 * nt * 16 * 4;
-    const uint32_t recv_bytes = cl > 1 ? fin_bytes * (cl - 1) : 0;
+    const int ranks = cl > 1 ? cl : 1;
+    const uint32_t red_unit_bytes = static_cast<uint32_t>(ranks * nred) * boxes * 8 * nt * red_stride * 4;
     const int budget = max_smem - 1024;
     const int max_slots = static_cast<int>((128u * 1024u) / slot_bytes) < 2 ? 2 : static_cast<int>((128u * 1024u) / slot_bytes);
     // Prefer 4 reduction buffers (owners of 4 consecutive units can hand in
@@ -91,15 +89,12 @@ inline bool plan_layout(int nt, int boxes, int nblk, int nblk_all, int xcols, in
             off += nss * ss_bytes;
             l.red = off;
             l.nrb = nrb;
+            l.nred_all = ranks * nred;
             off += red_bytes;
-            l.fin = off;
-            off += fin_bytes;
-            l.recv = off;
-            off += recv_bytes;
             l.bars = al(off, 8);
-            off = l.bars + 8 * (2 * nslot + 2 * nss + nrb + 4 + 3 + 1);
+            off = l.bars + 8 * (2 * nslot + 2 * nss + 3 + 1);
             l.tags = off;
-            off += 4 * (nslot + nss + 1 + 2 * nrb);
+            off += 4 * (nslot + nss + 2 * nrb);
             l.total = off;
             if (static_cast<int>(off) <= budget) {
                 *out = l;

@@ -37,7 +37,7 @@ inline int stage_steps(int boxes, int steps_a, int steps_b, int max_steps = 8) {
     return 1;
 }
 
-// Picks the deepest weight ring (<= 128 KB, >= 2 stages) that fits next to
+// Picks the deepest weight ring (<= 192 KB, >= 2 stages) that fits next to
 // the staged activations; the scale ring is deep enough that the producer is
 // never held back by it. Returns false if nothing fits.
 // nblk is the number of 32-blocks this CTA stages (its part of K); nblk_all
@@ -60,7 +60,7 @@ inline bool plan_layout(int nt, int boxes, int nblk, int nblk_all, int xcols, in
     const int ranks = cl > 1 ? cl : 1;
     const uint32_t red_unit_bytes = static_cast<uint32_t>(ranks * nred) * boxes * 8 * nt * red_stride * 4;
     const int budget = max_smem - 1024;
-    const int max_slots = static_cast<int>((128u * 1024u) / slot_bytes) < 2 ? 2 : static_cast<int>((128u * 1024u) / slot_bytes);
+    const int max_slots = static_cast<int>((192u * 1024u) / slot_bytes) < 2 ? 2 : static_cast<int>((192u * 1024u) / slot_bytes);
     // Prefer 4 reduction buffers (owners of 4 consecutive units can hand in
     // their partials without waiting) while the ring keeps >= 4 slots.
     for (int pass = 0; pass < 2; ++pass) {

@@ -198,9 +198,13 @@ __device__ __forceinline__ bool stage_bulk(const typename P::Params& p, int chun
                                 static_cast<uint32_t>(nb * 64), xfull);
     }
     if (!__all_sync(0xffffffffu, mbar_wait(xfull, parity, wc))) return false;
+    // Consecutive threads take consecutive columns of one block: the padded
+    // column stride puts them 4 banks apart, so a warp's 16-byte accesses
+    // need 4 wavefronts for T >= 4 (consecutive blocks of one column, 64
+    // bytes apart, would need 16).
     for (int it = tid; it < ncol * nb; it += nthreads) {
-        const int t = it / nb;
-        const int b = it - t * nb;
+        const int b = it / ncol;
+        const int t = it - b * ncol;
         const uint32_t a = xs_s + t * dst.xs_stride + b * 64;
         uint32_t w[16];
 #pragma unroll

@@ -125,55 +125,75 @@ __device__ int block_exclusive_scan(int v, int* warp_tot, int* total) {
     return before;
 }
 
+// Top-k of one token's E logits by one warp: lane l holds experts l, l + 32,
+// ... (NV per lane, E <= 32 * NV) in registers. Order: larger logit first,
+// ties to the smaller index; NaN never beats a number, and if only NaN
+// logits remain the smallest free index is taken.
+template <int NV>
+__device__ __forceinline__ void warp_topk(const float* row, int E, int top_k, int lane, float (&sel_v)[16],
+                                          int (&sel_i)[16]) {
+    float v[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] = (lane + 32 * i < E) ? row[lane + 32 * i] : 0.f;
+    uint32_t free_mask = 0;  // bit i: expert lane + 32 i exists and is not taken yet
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+        if (lane + 32 * i < E) free_mask |= 1u << i;
+    for (int j = 0; j < top_k; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int c = lane + 32 * i;
+            if ((free_mask >> i) & 1u)
+                if (better(v[i], c, bv, bi)) {
+                    bv = v[i];
+                    bi = c;
+                }
+        }
+#pragma unroll
+        for (int d = 16; d > 0; d >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, d);
+            if (better(ov, oi, bv, bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if (bi == 0x7fffffff) {  // only NaN logits left: take the smallest free index
+            int mine = free_mask ? lane + 32 * (__ffs(free_mask) - 1) : 0x7fffffff;
+#pragma unroll
+            for (int d = 16; d > 0; d >>= 1) mine = min(mine, __shfl_xor_sync(0xffffffffu, mine, d));
+            bi = mine;
+            bv = row[bi];
+        }
+        if ((bi & 31) == lane) free_mask &= ~(1u << (bi >> 5));
+        sel_v[j] = bv;
+        sel_i[j] = bi;
+    }
+}
+
 __global__ void __launch_bounds__(kRouteThreads, 1)
     moe_route_kernel(const float* __restrict__ logits, int T, int E, int top_k, MoeWork w, int32_t* topk_ids,
                      float* topk_w) {
     extern __shared__ int route_smem[];
     const int P = T * top_k;
-    int* s_ids = route_smem;                      // [P]
-    uint32_t* s_taken = reinterpret_cast<uint32_t*>(s_ids + P);  // [32 warps][32 words]
+    int* s_ids = route_smem;  // [P], then two [E] tables (see below)
     __shared__ int warp_tot[32];
     __shared__ int totals[3];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
     // Top-k and softmax: one warp per token.
-    uint32_t* taken = s_taken + warp * 32;
     for (int t = warp; t < T; t += kRouteThreads / 32) {
-        taken[lane] = 0;
-        __syncwarp();
         const float* row = logits + (size_t)t * E;
         float sel_v[16];
         int sel_i[16];
-        for (int j = 0; j < top_k; ++j) {
-            float bv = -INFINITY;
-            int bi = 0x7fffffff;
-            for (int c = lane; c < E; c += 32) {
-                if (taken[c >> 5] & (1u << (c & 31))) continue;
-                const float v = row[c];
-                if (better(v, c, bv, bi)) {
-                    bv = v;
-                    bi = c;
-                }
-            }
-#pragma unroll
-            for (int d = 16; d > 0; d >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, d);
-                const int oi = __shfl_xor_sync(0xffffffffu, bi, d);
-                if (better(ov, oi, bv, bi)) {
-                    bv = ov;
-                    bi = oi;
-                }
-            }
-            if (bi == 0x7fffffff) {  // only NaN logits left: take the smallest free index
-                bi = 0;
-                while (taken[bi >> 5] & (1u << (bi & 31))) ++bi;
-                bv = row[bi];
-            }
-            if (lane == 0) taken[bi >> 5] |= 1u << (bi & 31);
-            __syncwarp();
-            sel_v[j] = bv;
-            sel_i[j] = bi;
-        }
+        if (E <= 256)
+            warp_topk<8>(row, E, top_k, lane, sel_v, sel_i);
+        else if (E <= 512)
+            warp_topk<16>(row, E, top_k, lane, sel_v, sel_i);
+        else
+            warp_topk<32>(row, E, top_k, lane, sel_v, sel_i);
         if (lane == 0) {
             const float m = sel_v[0];
             float z = 0.f;
@@ -197,23 +217,44 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     __syncthreads();
 
     // Counting sort by expert; within an expert, pairs keep ascending order.
+    int* s_cnt = s_ids + P;  // [E]: pairs per expert, then the expert's first position
+    int* s_run = s_cnt + E;  // [E]: pairs of the expert placed so far
+    for (int i = threadIdx.x; i < E; i += kRouteThreads) {
+        s_cnt[i] = 0;
+        s_run[i] = 0;
+    }
+    __syncthreads();
+    for (int q = threadIdx.x; q < P; q += kRouteThreads) atomicAdd(&s_cnt[s_ids[q]], 1);  // order-free counts
+    __syncthreads();
     const int e = threadIdx.x;
-    int cnt = 0;
-    if (e < E)
-        for (int p = 0; p < P; ++p) cnt += (s_ids[p] == e);
+    const int cnt = e < E ? s_cnt[e] : 0;
     const int off = block_exclusive_scan(cnt, warp_tot, nullptr);
     const int n1 = (cnt + kChunkGateUp - 1) / kChunkGateUp;
     const int n2 = (cnt + kChunkDown - 1) / kChunkDown;
     const int c1 = block_exclusive_scan(n1, warp_tot, &totals[0]);
     const int c2 = block_exclusive_scan(n2, warp_tot, &totals[1]);
-    if (e < E && cnt > 0) {
-        int r = 0;
-        for (int p = 0; p < P; ++p)
-            if (s_ids[p] == e) {
-                w.sorted[off + r] = p;
-                w.pos[p] = off + r;
-                ++r;
+    if (e < E) s_cnt[e] = off;
+    __syncthreads();
+    // Positions: one warp walks the pairs in ascending order, 32 at a time;
+    // lanes holding the same expert are ranked by lane.
+    if (warp == 0) {
+        for (int base = 0; base < P; base += 32) {
+            const int q = base + lane;
+            const bool ok = q < P;
+            const int id = ok ? s_ids[q] : -1 - lane;  // distinct ids for idle lanes
+            const unsigned peers = __match_any_sync(0xffffffffu, id);
+            const int rank = __popc(peers & ((1u << lane) - 1u));
+            if (ok) {
+                const int at = s_cnt[id] + s_run[id] + rank;
+                w.sorted[at] = q;
+                w.pos[q] = at;
             }
+            __syncwarp();
+            if (ok && rank == 0) s_run[id] += __popc(peers);
+            __syncwarp();
+        }
+    }
+    if (e < E && cnt > 0) {
         for (int q = 0; q < n1; ++q) {
             w.c1_e[c1 + q] = e;
             w.c1_start[c1 + q] = off + q * kChunkGateUp;
@@ -427,7 +468,7 @@ int launch_moe(const uint8_t* w1q, const uint8_t* w2q, const MoeArgs& a, int num
                                 &d.tma3d))
         return rc;
 
-    const int route_smem = static_cast<int>(P * 4 + 32 * 32 * 4);
+    const int route_smem = static_cast<int>((P + 2 * a.E) * 4);
     if (route_smem > 48 * 1024) {
         if (cudaFuncSetAttribute(moe_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, route_smem) !=
             cudaSuccess)

@@ -334,22 +334,25 @@ struct DownParams {
     unsigned* status;
     int hidden, inter;
     int nblk, nkb, xcols, cl, tma3d;
-    int upc;             // units per chunk = hidden / 16
+    int upc;             // units per chunk = hidden / 32
     SmemLayout layout;
 };
 
+// A unit is 32 W2 rows of one expert (two boxes of 16 rows that share the
+// staged h columns): the per-unit costs (scale copy, hand-in, epilogue) are
+// spread over twice the weight bytes of a 16-row unit.
 struct DownProblem {
     static constexpr int NT = 1;
-    static constexpr int BOXES = 1;
-    static constexpr int NCW = 16;
+    static constexpr int BOXES = 2;
+    static constexpr int NCW = 11;  // 12 warps: up to 160 registers a thread
     using Params = DownParams;
 
     __device__ static int num_units(const Params& p) { return *(volatile const int*)&p.w.header[1] * p.upc; }
     __device__ static int chunk_of(const Params& p, int u) { return u / p.upc; }
-    __device__ static int box_row(const Params& p, int u, int) {
+    __device__ static int box_row(const Params& p, int u, int box) {
         const int q = u / p.upc;
         const int j = u - q * p.upc;
-        return p.w.c2_e[q] * p.hidden + 16 * j;
+        return p.w.c2_e[q] * p.hidden + 32 * j + 16 * box;
     }
     __device__ static const uint8_t* scale_src(const Params& p, int u, int box) {
         return p.w2s + (size_t)box_row(p, u, box) * p.nblk;
@@ -393,11 +396,13 @@ struct DownProblem {
         const int j = u - q * p.upc;
         const int cnt = p.w.c2_cnt[q];
         const int start = p.w.c2_start[q];
-        for (int e = lane; e < cnt * 16; e += 32) {
-            const int t = e >> 4;
-            const int r = e & 15;
-            p.w.o[(size_t)(start + t) * p.hidden + 16 * j + r] = v.sum(0, t, r) + v.sum(0, cnt + t, r);
-        }
+#pragma unroll
+        for (int bx = 0; bx < 2; ++bx)
+            for (int e = lane; e < cnt * 16; e += 32) {
+                const int t = e >> 4;
+                const int r = e & 15;
+                p.w.o[(size_t)(start + t) * p.hidden + 32 * j + 16 * bx + r] = v.sum(bx, t, r) + v.sum(bx, cnt + t, r);
+            }
     }
 };
 
@@ -452,11 +457,11 @@ int launch_moe(const uint8_t* w1q, const uint8_t* w2q, const MoeArgs& a, int num
     d.nblk = a.inter / 32;
     d.nkb = (a.inter + 255) / 256;
     d.xcols = 2 * kChunkDown;
-    d.upc = a.hidden / 16;
+    d.upc = a.hidden / 32;
     d.cl = 1;
-    const int steps2 = stage_steps(1, d.nkb, 0);
+    const int steps2 = stage_steps(2, d.nkb, 0);
     const int group2 = steps2 % 2 == 0 ? steps2 / 2 : steps2;
-    if (!plan_layout(1, 1, d.nblk, d.nblk, d.xcols, 1, DownProblem::NCW, kRedStride, steps2, group2, d.nkb,
+    if (!plan_layout(1, 2, d.nblk, d.nblk, d.xcols, 1, DownProblem::NCW, kRedStride, steps2, group2, d.nkb,
                      max_smem, &d.layout))
         return MXFP4_ERR_SHAPE;
 

@@ -287,7 +287,7 @@ struct GateUpParams {
 struct GateUpProblem {
     static constexpr int NT = 1;
     static constexpr int BOXES = 2;
-    static constexpr int NCW = 12;
+    static constexpr int NCW = 11;  // 12 warps: up to 160 registers a thread
     using Params = GateUpParams;
 
     __device__ static int num_units(const Params& p) { return *(volatile const int*)&p.w.header[0] * p.upc; }

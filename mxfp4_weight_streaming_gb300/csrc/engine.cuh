@@ -124,9 +124,14 @@ struct Pow2Scaler {
 
 // Stage one block of 32 bf16 values (16 words) as f16 column data.
 __device__ __forceinline__ void stage_bf16_block(const uint32_t (&w)[16], uint8_t* dst, float* fx_out) {
-    uint32_t amax = 0;
+    // Largest magnitude: a depth-4 tree of packed 16-bit maxima.
+    uint32_t m[8];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) amax = max(amax, max(w[j] & 0x7fffu, (w[j] >> 16) & 0x7fffu));
+    for (int j = 0; j < 8; ++j) m[j] = __vmaxu2(w[2 * j] & 0x7fff7fffu, w[2 * j + 1] & 0x7fff7fffu);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) m[j] = __vmaxu2(m[j], m[j + 4]);
+    m[0] = __vmaxu2(__vmaxu2(m[0], m[2]), __vmaxu2(m[1], m[3]));
+    const uint32_t amax = max(m[0] & 0xffffu, m[0] >> 16);
     int c = 0;
     if (amax != 0) c = staging_exponent(floor_log2_f32_bits(amax << 16));
     const Pow2Scaler sc(c);
@@ -136,9 +141,9 @@ __device__ __forceinline__ void stage_bf16_block(const uint32_t (&w)[16], uint8_
         __half2 h = __floats2half2_rn(sc(__uint_as_float(w[j] << 16)), sc(__uint_as_float(w[j] & 0xffff0000u)));
         o[j] = *reinterpret_cast<uint32_t*>(&h);
     }
-    uint4* d = reinterpret_cast<uint4*>(dst);
+    const uint32_t d = smem_addr(dst);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) d[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+    for (int q = 0; q < 4; ++q) sts128(d + 16 * q, o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
     *fx_out = exp2_int(-c);
 }
 

@@ -101,6 +101,24 @@ int encode_weights(CUtensorMap* map, const uint8_t* wq, int64_t rows, int64_t k,
 }
 }  // namespace mxfp4
 
+namespace {
+
+// Plans and TMA descriptors of recent linear calls, per host thread: a
+// layer calls with the same weights and shape every step, and the plan and
+// the descriptor (which embeds the weight address) depend on nothing else.
+struct LinearPlan {
+    int dev = -1;
+    const uint8_t* wq = nullptr;
+    int64_t t = 0, k = 0, n = 0;
+    mxfp4::LinearParams p{};
+    CUtensorMap map;
+};
+constexpr int kPlanCache = 16;
+thread_local LinearPlan t_plans[kPlanCache];
+thread_local int t_plan_next = 0;
+
+}  // namespace
+
 extern "C" {
 
 const char* mxfp4_strerror(int status) {
@@ -133,11 +151,31 @@ int mxfp4_linear(const void* x, int64_t t, int64_t k, const uint8_t* wq, const u
     if (!aligned(x, 16) || !aligned(wq, 16) || !aligned(ws, 16) || !aligned(y, 2)) return MXFP4_ERR_ALIGN;
     DeviceInfo* d = nullptr;
     if (int rc = device_info(&d)) return rc;
-    mxfp4::LinearParams p{};
-    if (!mxfp4::plan_linear(static_cast<int>(t), static_cast<int>(k), d->max_smem, &p.cl, &p.layout))
-        return MXFP4_ERR_SHAPE;
-    CUtensorMap map;
-    if (int rc = encode_weight_map(&map, wq, n, k, static_cast<int>(p.layout.steps), &p.tma3d)) return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    LinearPlan* plan = nullptr;
+    for (LinearPlan& c : t_plans)
+        if (c.dev == dev && c.wq == wq && c.t == t && c.k == k && c.n == n) {
+            plan = &c;
+            break;
+        }
+    if (!plan) {
+        LinearPlan fresh;
+        if (!mxfp4::plan_linear(static_cast<int>(t), static_cast<int>(k), d->max_smem, &fresh.p.cl, &fresh.p.layout))
+            return MXFP4_ERR_SHAPE;
+        if (int rc = encode_weight_map(&fresh.map, wq, n, k, static_cast<int>(fresh.p.layout.steps), &fresh.p.tma3d))
+            return rc;
+        fresh.dev = dev;
+        fresh.wq = wq;
+        fresh.t = t;
+        fresh.k = k;
+        fresh.n = n;
+        plan = &t_plans[t_plan_next];
+        t_plan_next = (t_plan_next + 1) % kPlanCache;
+        *plan = fresh;
+    }
+    mxfp4::LinearParams p = plan->p;
+    const CUtensorMap& map = plan->map;
     p.x = static_cast<const __nv_bfloat16*>(x);
     p.ws = ws;
     p.y = static_cast<__nv_bfloat16*>(y);

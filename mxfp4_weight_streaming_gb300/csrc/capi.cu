@@ -161,7 +161,9 @@ int mxfp4_linear(const void* x, int64_t t, int64_t k, const uint8_t* wq, const u
         }
     if (!plan) {
         LinearPlan fresh;
-        if (!mxfp4::plan_linear(static_cast<int>(t), static_cast<int>(k), d->max_smem, &fresh.p.cl, &fresh.p.layout))
+        const bool few_units = (n + 15) / 16 <= 4 * static_cast<int64_t>(d->num_sms);
+        if (!mxfp4::plan_linear(static_cast<int>(t), static_cast<int>(k), d->max_smem, few_units, &fresh.p.cl,
+                                &fresh.p.layout))
             return MXFP4_ERR_SHAPE;
         if (int rc = encode_weight_map(&fresh.map, wq, n, k, static_cast<int>(fresh.p.layout.steps), &fresh.p.tma3d))
             return rc;

@@ -55,7 +55,18 @@ struct DenseProblem {
 
 static int tokens_to_nt(int T) { return T <= 8 ? 1 : (T <= 16 ? 2 : 4); }
 
-bool plan_linear(int T, int K, int max_smem, int* cl, SmemLayout* L) {
+// few_units: at most 4 row groups per SM. Whole-stage chunks would then leave
+// most consumer warps idle, so stages are capped at 4 K steps (more, smaller
+// chunks); larger problems keep 7-8 step stages (larger copies, fewer
+// handshakes).
+static bool plan_linear_steps(int T, int K, int max_smem, int max_steps, int* cl, SmemLayout* L);
+
+bool plan_linear(int T, int K, int max_smem, bool few_units, int* cl, SmemLayout* L) {
+    if (few_units && plan_linear_steps(T, K, max_smem, 4, cl, L)) return true;
+    return plan_linear_steps(T, K, max_smem, 8, cl, L);  // (also when the smaller stages fit no layout)
+}
+
+static bool plan_linear_steps(int T, int K, int max_smem, int max_steps, int* cl, SmemLayout* L) {
     const int nblk = K / 32;
     const int nkb = (K + 255) / 256;
     for (int c = 1; c <= 8; c *= 2) {
@@ -78,7 +89,7 @@ bool plan_linear(int T, int K, int max_smem, int* cl, SmemLayout* L) {
             }
             g = a;
         }
-        const int steps = stage_steps(1, g, 0);
+        const int steps = stage_steps(1, g, 0, max_steps);
         if (plan_layout(nt, 1, nb_local, nblk, T, c, ncw, kRedStride, steps, steps, nkb_c, max_smem, L)) {
             *cl = c;
             return true;

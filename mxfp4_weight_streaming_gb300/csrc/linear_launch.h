@@ -27,7 +27,7 @@ struct LinearParams {
 
 // Chooses the cluster size (1, 2, 4 or 8 CTAs splitting K) and the shared
 // memory plan; false if no plan fits.
-bool plan_linear(int T, int K, int max_smem, int* cl, SmemLayout* L);
+bool plan_linear(int T, int K, int max_smem, bool few_units, int* cl, SmemLayout* L);
 cudaError_t launch_linear(const CUtensorMap& tmap, const LinearParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_quantize(const float* w, int64_t n, int64_t k, uint8_t* wq, uint8_t* ws, cudaStream_t stream,
                             int num_sms);

@@ -459,8 +459,10 @@ int launch_moe(const uint8_t* w1q, const uint8_t* w2q, const MoeArgs& a, int num
     d.xcols = 2 * kChunkDown;
     d.upc = a.hidden / 32;
     d.cl = 1;
+    // Down: a consumer warp takes whole stages (measured faster than half
+    // stages here; gate/up is faster with half stages).
     const int steps2 = stage_steps(2, d.nkb, 0);
-    const int group2 = steps2 % 2 == 0 ? steps2 / 2 : steps2;
+    const int group2 = steps2;
     if (!plan_layout(1, 2, d.nblk, d.nblk, d.xcols, 1, DownProblem::NCW, kRedStride, steps2, group2, d.nkb,
                      max_smem, &d.layout))
         return MXFP4_ERR_SHAPE;

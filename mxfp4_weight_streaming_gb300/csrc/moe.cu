@@ -440,8 +440,8 @@ int launch_moe(const uint8_t* w1q, const uint8_t* w2q, const MoeArgs& a, int num
     g.xcols = kChunkGateUp;
     g.upc = a.inter / 16;
     g.cl = 1;
-    // Consumer chunks of half a stage keep every consumer warp supplied from
-    // the ring (8 stages of 16 KB hold 16 chunks for 12 warps).
+    // Gate/up: consumer chunks of half a stage (measured faster than whole
+    // stages here: more chunks in flight for the 11 consumer warps).
     const int steps1 = stage_steps(2, g.nkb, 0);
     const int group1 = steps1 % 2 == 0 ? steps1 / 2 : steps1;
     if (!plan_layout(1, 2, g.nblk, g.nblk, g.xcols, 1, GateUpProblem::NCW, kRedStride, steps1, group1, g.nkb,

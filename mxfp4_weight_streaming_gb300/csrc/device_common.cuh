@@ -123,24 +123,6 @@ __device__ __forceinline__ uint32_t atom_add_shared(uint32_t a, uint32_t v) {
     return old;
 }
 
-// Waits until the shared counter at addr is >= want.
-__device__ __forceinline__ bool wait_shared_at_least(uint32_t addr, uint32_t want, const WaitCtx& w) {
-    if (lds_u32_volatile(addr) >= want) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
-        if (*w.abort) return false;
-#pragma unroll 1
-        for (int i = 0; i < 32; ++i) {
-            __nanosleep(32);
-            if (lds_u32_volatile(addr) >= want) return true;
-        }
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
-            record_timeout(w);
-            return false;
-        }
-    }
-}
-
 // ------------------------------------------- programmatic dependent launch
 // Lets the next kernel of the stream be scheduled before this one ends (its
 // CTAs become resident as SMs free up).
@@ -196,49 +178,9 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
-// Arrive on an mbarrier of another CTA of the cluster, releasing this
-// thread's earlier writes at cluster scope.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
-// Arrive on an mbarrier of another CTA of the cluster without ordering
-// this thread's memory accesses (for "buffer free again" signals whose
-// reads have already completed).
-__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
 // Makes this thread's earlier writes (and those ordered before them, e.g.
 // by a warp barrier) visible cluster-wide before its later writes.
 __device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
-
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait on a local mbarrier that other CTAs of the cluster arrive on.
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, const WaitCtx& w) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
-        if (*w.abort) return false;
-#pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait_cluster(bar, parity)) return true;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
-            record_timeout(w);
-            return false;
-        }
-    }
-}
 
 // Whole-cluster barrier (every thread of every CTA).
 __device__ __forceinline__ void cluster_sync_all() {
@@ -316,12 +258,6 @@ __device__ __forceinline__ uint2 lds64(uint32_t a) {
     return v;
 }
 
-__device__ __forceinline__ float2 lds64f(uint32_t a) {
-    float2 v;
-    asm volatile("ld.shared.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a));
-    return v;
-}
-
 __device__ __forceinline__ uint64_t lds64_pair(uint32_t a) {
     uint64_t v;
     asm volatile("ld.shared.b64 %0, [%1];" : "=l"(v) : "r"(a));
@@ -345,16 +281,6 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                  : "r"(addr));
-}
-
-// D = A(16x16 f16) * B(16x8 f16) + C, fp32 accumulate.
-__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                              uint32_t b0, uint32_t b1, const float (&c)[4]) {
-    asm(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%10,%11,%12,%13};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
 }
 
 // The two chained m16n8k16 products of one 32-block: A holds the 16 rows'
@@ -432,12 +358,6 @@ __device__ __forceinline__ void e2m1x8_to_f16x8(uint32_t v, uint32_t& o0, uint32
         "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
         : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3)
         : "r"(v));
-}
-
-// 2^(s-127) for an E8M0 byte s in [0, 254], exact (s = 0 is the float32
-// subnormal 2^-127).
-__device__ __forceinline__ float e8m0_to_float(uint32_t s) {
-    return __int_as_float(max(static_cast<int>(s << 23), 0x00400000));
 }
 
 // 2^e as float32 for e in [-149, 127], exact.

@@ -161,9 +161,12 @@ int mxfp4_linear(const void* x, int64_t t, int64_t k, const uint8_t* wq, const u
         }
     if (!plan) {
         LinearPlan fresh;
-        const bool few_units = (n + 15) / 16 <= 4 * static_cast<int64_t>(d->num_sms);
-        if (!mxfp4::plan_linear(static_cast<int>(t), static_cast<int>(k), d->max_smem, few_units, &fresh.p.cl,
-                                &fresh.p.layout))
+        const int64_t n_rg = (n + 15) / 16;
+        const bool few_units = n_rg <= 4 * static_cast<int64_t>(d->num_sms);
+        const int64_t ctas = n_rg < d->num_sms ? n_rg : d->num_sms;
+        const int units_per_cta = static_cast<int>((n_rg + ctas - 1) / ctas);
+        if (!mxfp4::plan_linear(static_cast<int>(t), static_cast<int>(k), d->max_smem, few_units, units_per_cta,
+                                &fresh.p.cl, &fresh.p.layout))
             return MXFP4_ERR_SHAPE;
         if (int rc = encode_weight_map(&fresh.map, wq, n, k, static_cast<int>(fresh.p.layout.steps), &fresh.p.tma3d))
             return rc;

@@ -58,10 +58,13 @@ struct Bars {
     __device__ uint32_t empty(uint32_t s) const { return base + 8 * (nslot + s); }
     __device__ uint32_t sfull(uint32_t s) const { return base + 8 * (2 * nslot + s); }
     __device__ uint32_t sempty(uint32_t s) const { return base + 8 * (2 * nslot + nss + s); }
-    // xbar(0), xbar(1): all consumers before / after staging; xbar(2): the
-    // bulk copies of raw activations have landed.
+    // Whole-K staging: xbar(0), xbar(1): all consumers before / after
+    // staging; xbar(2): the bulk copies of raw activations have landed.
+    // K in parts: xbar(b) (b = 0, 1): the raw activations of a part have
+    // landed in buffer b; xbar(2 + b): every consumer has converted its
+    // share of buffer b.
     __device__ uint32_t xbar(uint32_t b) const { return base + 8 * (2 * nslot + 2 * nss + b); }
-    __device__ uint32_t abort_flag() const { return base + 8 * (2 * nslot + 2 * nss + 3); }
+    __device__ uint32_t abort_flag() const { return base + 8 * (2 * nslot + 2 * nss + 5); }
     // Stage last issued into ring slot s; unit last issued into scale slot s.
     __device__ uint32_t ring_tag(uint32_t s) const { return tags + 4 * s; }
     __device__ uint32_t scale_tag(uint32_t s) const { return tags + 4 * (nslot + s); }
@@ -70,6 +73,10 @@ struct Bars {
     // count on rank 0 is the one used).
     __device__ uint32_t red_tag(uint32_t b) const { return tags + 4 * (nslot + nss + b); }
     __device__ uint32_t red_count(uint32_t b) const { return tags + 4 * (nslot + nss + nrb + b); }
+    // K in parts: consumer warps that have left the part in buffer b.
+    __device__ uint32_t xdone(uint32_t b) const { return tags + 4 * (nslot + nss + 2 * nrb + b); }
+    // K in parts: copies issued into buffer b so far.
+    __device__ uint32_t xissued(uint32_t b) const { return tags + 4 * (nslot + nss + 2 * nrb + 2 + b); }
 };
 
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx& w) {
@@ -187,22 +194,28 @@ __device__ __forceinline__ void stage_f32_block_split(const float (&v)[32], uint
 // layout is the same: 64 bytes per 32-block), then every consumer thread
 // converts blocks in place. Only shared-memory latency is on the path,
 // instead of one dependent global load per block and thread.
+
+// One thread: the copies of a chunk's columns into the columns at xs_s,
+// completing on the transaction barrier xfull.
 template <class P>
-__device__ __forceinline__ bool stage_bulk(const typename P::Params& p, int chunk, int kblk0, int kblk1,
-                                           const StageDst& dst, uint32_t xs_s, uint32_t xfull, uint32_t parity,
-                                           const WaitCtx& wc, int tid, int nthreads) {
-    constexpr int kCols = 8 * P::NT;  // staged tile width (columns)
+__device__ __forceinline__ void issue_column_copies(const typename P::Params& p, int chunk, int kblk0, int kblk1,
+                                                    uint32_t xs_s, uint32_t xs_stride, uint32_t xfull) {
     const int ncol = P::stage_cols(p, chunk);
     const int nb = kblk1 - kblk0;
-    if (tid == 0) {
-        fence_proxy_async_shared();  // earlier reads / writes of the columns come first
-        mbar_arrive_expect_tx(xfull, static_cast<uint32_t>(ncol * nb * 64));
-        if (nb > 0)
-            for (int t = 0; t < ncol; ++t)
-                bulk_load_plain(xs_s + t * dst.xs_stride, P::stage_row(p, chunk, t) + static_cast<size_t>(kblk0) * 64,
-                                static_cast<uint32_t>(nb * 64), xfull);
-    }
-    if (!__all_sync(0xffffffffu, mbar_wait(xfull, parity, wc))) return false;
+    fence_proxy_async_shared();  // earlier reads / writes of the columns come first
+    mbar_arrive_expect_tx(xfull, static_cast<uint32_t>(ncol * nb * 64));
+    if (nb > 0)
+        for (int t = 0; t < ncol; ++t)
+            bulk_load_plain(xs_s + t * xs_stride, P::stage_row(p, chunk, t) + static_cast<size_t>(kblk0) * 64,
+                            static_cast<uint32_t>(nb * 64), xfull);
+}
+
+// Thread tid of nthreads: converts its share of the landed bf16 blocks of
+// ncol columns (nb blocks each) in place, and zeroes the factors of the
+// tile's unused columns (kCols = 8 * NT).
+template <int kCols>
+__device__ __forceinline__ void convert_columns(int ncol, int nb, const StageDst& dst, uint32_t xs_s, int tid,
+                                                int nthreads) {
     // Consecutive threads take consecutive columns of one block: the padded
     // column stride puts them 4 banks apart, so a warp's 16-byte accesses
     // need 4 wavefronts for T >= 4 (consecutive blocks of one column, 64
@@ -222,11 +235,20 @@ __device__ __forceinline__ bool stage_bulk(const typename P::Params& p, int chun
         }
         stage_bf16_block(w, dst.col(t, b), dst.factor(t, b));
     }
-    // Factors of the unused columns of the tile are zero.
     for (int it = tid; it < nb * (kCols - ncol); it += nthreads) {
         const int b = it / (kCols - ncol);
         *dst.factor(ncol + (it - b * (kCols - ncol)), b) = 0.0f;
     }
+}
+
+// Whole-K staging of one chunk: copy, wait, convert (all consumer threads).
+template <class P>
+__device__ __forceinline__ bool stage_bulk(const typename P::Params& p, int chunk, int kblk0, int kblk1,
+                                           const StageDst& dst, uint32_t xs_s, uint32_t xfull, uint32_t parity,
+                                           const WaitCtx& wc, int tid, int nthreads) {
+    if (tid == 0) issue_column_copies<P>(p, chunk, kblk0, kblk1, xs_s, dst.xs_stride, xfull);
+    if (!__all_sync(0xffffffffu, mbar_wait(xfull, parity, wc))) return false;
+    convert_columns<8 * P::NT>(P::stage_cols(p, chunk), kblk1 - kblk0, dst, xs_s, tid, nthreads);
     return true;
 }
 
@@ -392,6 +414,64 @@ struct Placement {
     uint32_t rank, cl;
 };
 
+// One item of a CTA's work: the K steps [kb0, kb1) of one unit. Without K
+// parts an item is a whole unit over the CTA's K range.
+struct Item {
+    int u;           // unit
+    uint32_t uu;     // unit ordinal within the CTA (scale-slot sequence)
+    uint32_t j;      // unit ordinal within its batch (carry slot)
+    int part;        // K part (0 without parts)
+    bool last;       // last part of the unit
+    int q;           // K parts: activation chunk = batch * nparts + part
+    int kb0, kb1;    // K steps (256 values each)
+    int kblk0, kblk1;  // 32-blocks
+};
+
+// The CTA's items in streaming order. K in parts (ps > 0): units are taken
+// in batches of ub; for each part, that part of every unit of the batch.
+struct ItemSeq {
+    int u0, nu;
+    int ps, nparts, ub;
+    int nkb, nblk;
+    int kb0, kb1, kblk0, kblk1;  // the CTA's K range without parts
+    __device__ int count() const { return ps ? nu * nparts : nu; }
+    __device__ int nchunks() const { return ps ? ((nu + ub - 1) / ub) * nparts : 0; }
+    __device__ void part_blocks(int part, int& b0, int& b1) const {
+        b0 = part * ps * 8;
+        b1 = min(nblk, (part + 1) * ps * 8);
+    }
+    __device__ Item at(int v) const {
+        Item it;
+        if (!ps) {
+            it.u = u0 + v;
+            it.uu = static_cast<uint32_t>(v);
+            it.j = 0;
+            it.part = 0;
+            it.last = true;
+            it.q = 0;
+            it.kb0 = kb0;
+            it.kb1 = kb1;
+            it.kblk0 = kblk0;
+            it.kblk1 = kblk1;
+            return it;
+        }
+        // Every batch but the last is full, so the batch is v / (ub * nparts).
+        const int bi = v / (ub * nparts);
+        const int r = v - bi * ub * nparts;
+        const int bsize = min(ub, nu - bi * ub);
+        it.part = r / bsize;
+        it.j = static_cast<uint32_t>(r - it.part * bsize);
+        it.uu = static_cast<uint32_t>(bi * ub) + it.j;
+        it.u = u0 + static_cast<int>(it.uu);
+        it.last = it.part == nparts - 1;
+        it.q = bi * nparts + it.part;
+        it.kb0 = it.part * ps;
+        it.kb1 = min(nkb, it.kb0 + ps);
+        part_blocks(it.part, it.kblk0, it.kblk1);
+        return it;
+    }
+};
+
 // ------------------------------------------------------------------------
 // Shared-memory carve-up of one CTA (offsets from the 1024-aligned base).
 struct Smem {
@@ -476,6 +556,99 @@ __device__ void producer_role(const typename P::Params& p, const Smem& S, const 
                     for (int bx = 0; bx < BOXES; ++bx)
                         tma_load_2d(sbase + (bx * spb + j) * kBoxBytes, tmap, kb * 128, rows[bx], bars.full(slot),
                                     policy);
+                }
+            }
+            ++staged;
+        }
+    }
+    if (!ok) {
+        // Let every copy still in flight land (bounded) before the CTA exits.
+        // These waits ignore the abort flag: copies complete on their own.
+        int never = 0;
+        const WaitCtx own{p.status, &never};
+        const uint32_t first = staged > L.nslot ? staged - L.nslot : 0;
+        for (uint32_t j = first; j < staged; ++j) mbar_wait(bars.full(j % L.nslot), (j / L.nslot) & 1, own);
+        const uint32_t sfirst = sissued > L.nss ? sissued - L.nss : 0;
+        for (uint32_t j = sfirst; j < sissued; ++j) mbar_wait(bars.sfull(j % L.nss), (j / L.nss) & 1, own);
+    }
+}
+
+template <class P>
+__device__ void producer_parts(const typename P::Params& p, const Smem& S, const Placement& pl, const ItemSeq& seq,
+                               const CUtensorMap* tmap, int lane) {
+    // producer_role over the items of K in parts: a unit's scales (all of
+    // K) are copied with its first part and serve every part; the stages of
+    // each item follow in streaming order.
+    if (lane != 0) return;
+    constexpr int BOXES = P::BOXES;
+    const SmemLayout& L = S.L;
+    const Bars& bars = S.bars;
+    const uint32_t spb = L.steps;
+    const uint32_t stage_bytes = spb * BOXES * kBoxBytes;
+    const uint32_t scale_bytes = 16u * static_cast<uint32_t>(p.nblk);
+    if (pl.kb1 - pl.kb0 <= 0) return;  // a cluster rank with no part of K: nothing to stream
+    const uint64_t policy = l2_evict_first_policy();
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+    bool ok = true;
+    uint32_t staged = 0, sissued = 0;
+    const int ni = seq.count();
+    for (int v = 0; v < ni && ok; ++v) {
+        const Item it = seq.at(v);
+        const int u = it.u;
+        const uint32_t uu = it.uu;
+        if (it.part == 0) {
+            const uint32_t ss = uu % L.nss;
+            if (!mbar_wait(bars.sempty(ss), ((uu / L.nss) & 1) ^ 1, S.wait)) {
+                ok = false;
+                break;
+            }
+            sts_u32_volatile(bars.scale_tag(ss), uu);  // the slot now belongs to unit uu
+            // Scale rows of the unit: a bulk copy of the 16-byte-aligned part, and
+            // (only for a tail row group) the last few bytes stored by this lane.
+            const uint32_t bytes = static_cast<uint32_t>(P::unit_rows(p, u)) * static_cast<uint32_t>(p.nblk);
+            const uint32_t bulk = bytes & ~15u;
+            const uint32_t dst = S.base + L.sc + ss * L.ss_bytes;
+            uint8_t* dst_g = S.gbase + L.sc + ss * L.ss_bytes;
+#pragma unroll
+            for (int bx = 0; bx < BOXES; ++bx) {
+                const uint8_t* src = P::scale_src(p, u, bx);
+                for (uint32_t b = bulk; b < bytes; ++b) dst_g[bx * scale_bytes + b] = src[b];
+            }
+            mbar_arrive_expect_tx(bars.sfull(ss), bulk * BOXES);
+            if (bulk) {
+#pragma unroll
+                for (int bx = 0; bx < BOXES; ++bx)
+                    bulk_load(dst + bx * scale_bytes, P::scale_src(p, u, bx), bulk, bars.sfull(ss), policy);
+            }
+            ++sissued;
+        }
+        int rows[BOXES];
+#pragma unroll
+        for (int bx = 0; bx < BOXES; ++bx) rows[bx] = P::box_row(p, u, bx);
+        for (int kb = it.kb0; kb < it.kb1; kb += static_cast<int>(spb)) {
+            const uint32_t slot = staged % L.nslot;
+            if (!mbar_wait(bars.empty(slot), ((staged / L.nslot) & 1) ^ 1, S.wait)) {
+                ok = false;
+                break;
+            }
+            // The slot now belongs to stage `staged`: its previous stage has
+            // been consumed, so a consumer that sees this tag can wait on the
+            // slot's full barrier without mistaking an older phase for it.
+            sts_u32_volatile(bars.ring_tag(slot), staged);
+            mbar_arrive_expect_tx(bars.full(slot), stage_bytes);
+            // Stage layout: [box][step][16 rows][128 B], 128-byte swizzle.
+            const uint32_t sbase = S.base + L.ring + slot * stage_bytes;
+            if (p.tma3d) {
+                // One copy per box: 16 rows x spb 128-byte segments of K.
+#pragma unroll
+                for (int bx = 0; bx < BOXES; ++bx)
+                    tma_load_3d(sbase + bx * spb * kBoxBytes, tmap, 0, rows[bx], kb, bars.full(slot), policy);
+            } else {
+                for (uint32_t j = 0; j < spb; ++j) {
+#pragma unroll
+                    for (int bx = 0; bx < BOXES; ++bx)
+                        tma_load_2d(sbase + (bx * spb + j) * kBoxBytes, tmap, (kb + static_cast<int>(j)) * 128,
+                                    rows[bx], bars.full(slot), policy);
                 }
             }
             ++staged;
@@ -705,6 +878,142 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
     }
 }
 
+// K in parts (lone CTA): the units of a batch belong to one warp each (warp
+// j takes unit j of every batch; ub <= NCW), so a unit's accumulators stay
+// in that warp's registers across all parts and its epilogue runs once.
+// Every consumer warp, owner or not, takes part in staging each part's
+// activations: the part's buffer (q & 1 for chunk q = batch * nparts + part)
+// was filled by a copy that the last warp to leave chunk q - 2 issued (the
+// first thread issues chunks 0 and 1); each warp converts its share, and all
+// shares are done before any warp reads the buffer.
+template <class P>
+__device__ void consumer_parts(const typename P::Params& p, const Smem& S, const ItemSeq& seq, int warp, int lane) {
+    constexpr int NT = P::NT;
+    constexpr int BOXES = P::BOXES;
+    constexpr int kRedWarpFloats = BOXES * 8 * NT * kRedStride;
+    const SmemLayout& L = S.L;
+    const Bars& bars = S.bars;
+    const uint32_t spb = L.steps;
+    const uint32_t stage_bytes = spb * BOXES * kBoxBytes;
+    const uint32_t box_stride = spb * kBoxBytes;
+    const uint32_t spi = L.part_steps / spb;  // stages per item
+    uint8_t* xs = S.gbase + L.xs;
+    uint8_t* fx = S.gbase + L.fx;
+    float* red = reinterpret_cast<float*>(S.gbase + L.red) + warp * kRedWarpFloats;  // this warp's slot
+    const uint32_t xs_s = S.base + L.xs, fx_s = S.base + L.fx, scb = S.base + L.sc, ring = S.base + L.ring;
+    const int tid = warp * 32 + lane;
+    const bool fast_steps = (p.nblk & 7) == 0;  // 8-byte aligned scale words
+    const int ncols = P::ncols(p, 0);
+    const int nq = seq.nchunks();
+    pdl_wait_previous();  // activations may come from the previous kernel
+    if (tid == 0) {
+        for (int q0 = 0; q0 < 2 && q0 < nq; ++q0) {
+            int b0, b1;
+            seq.part_blocks(q0 % seq.nparts, b0, b1);
+            sts_u32_volatile(bars.xissued(q0), 1u);
+            issue_column_copies<P>(p, 0, b0, b1, xs_s + q0 * L.xs_buf, L.xs_stride, bars.xbar(q0));
+        }
+    }
+    int q = 0;
+    const int nbatch = (seq.nu + seq.ub - 1) / seq.ub;
+    for (int bi = 0; bi < nbatch; ++bi) {
+        const int bsize = min(seq.ub, seq.nu - bi * seq.ub);
+        const bool own = warp < bsize;
+        const uint32_t uu = static_cast<uint32_t>(bi * seq.ub + warp);
+        const uint32_t ss = uu % L.nss;
+        uint64_t acc[BOXES][NT][2];
+#pragma unroll
+        for (int bx = 0; bx < BOXES; ++bx)
+#pragma unroll
+            for (int n = 0; n < NT; ++n) acc[bx][n][0] = acc[bx][n][1] = 0ull;  // +0.0f pairs
+        for (int part = 0; part < seq.nparts; ++part, ++q) {
+            if (q > 0) {
+                // This warp has left chunk q - 1: the last warp out reloads
+                // that buffer with chunk q + 1.
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t b = static_cast<uint32_t>(q - 1) & 1u;
+                    __threadfence_block();  // this warp's reads of the buffer come first
+                    if (atom_add_shared(bars.xdone(b), 1u) == static_cast<uint32_t>(P::NCW - 1)) {
+                        sts_u32_volatile(bars.xdone(b), 0u);
+                        if (q + 1 < nq) {
+                            __threadfence_block();
+                            int b0, b1;
+                            seq.part_blocks((q + 1) % seq.nparts, b0, b1);
+                            sts_u32_volatile(bars.xissued(b), lds_u32_volatile(bars.xissued(b)) + 1u);
+                            issue_column_copies<P>(p, 0, b0, b1, xs_s + b * L.xs_buf, L.xs_stride, bars.xbar(b));
+                        }
+                    }
+                }
+            }
+            int kblk0, kblk1;
+            seq.part_blocks(part, kblk0, kblk1);
+            const uint32_t b = static_cast<uint32_t>(q) & 1u;
+            const uint32_t par = (static_cast<uint32_t>(q) >> 1) & 1u;
+            if (!warp_wait(bars.xbar(b), par, S.wait)) return;
+            const StageDst dst{xs + b * L.xs_buf, fx + b * L.fx_buf, L.xs_stride, L.fx_stride};
+            convert_columns<8 * NT>(P::stage_cols(p, 0), kblk1 - kblk0, dst, xs_s + b * L.xs_buf, tid,
+                                    Roles<P>::kConsumerThreads);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.xbar(2 + b));
+            if (!warp_wait(bars.xbar(2 + b), par, S.wait)) return;
+            if (!own) continue;
+            if (part == 0) {
+                // The unit's scales (all of K) arrive with its first part.
+                if (!__all_sync(0xffffffffu, wait_shared_value(bars.scale_tag(ss), uu, S.wait))) return;
+                if (!warp_wait(bars.sfull(ss), (uu / L.nss) & 1, S.wait)) return;
+            }
+            const uint32_t sc = scb + ss * L.ss_bytes;
+            const uint32_t xcur = xs_s + b * L.xs_buf, fcur = fx_s + b * L.fx_buf;
+            // The producer streams item (batch, part, unit) as item number
+            // v = (batch * nparts + part) * ub + unit of a full batch (the
+            // last batch has bsize units), spi stages each.
+            const uint32_t v = static_cast<uint32_t>(bi * seq.ub * seq.nparts + part * bsize + warp);
+            uint32_t stage = v * spi;
+            int kb = part * seq.ps;
+            for (uint32_t s = 0; s < spi; ++s, ++stage) {
+                const uint32_t slot = stage % L.nslot;
+                const uint32_t phase = (stage / L.nslot) & 1u;
+                // The tag says the producer has claimed the slot for this
+                // stage, so the parity wait refers to this stage's phase.
+                if (!__all_sync(0xffffffffu, wait_shared_value(bars.ring_tag(slot), stage, S.wait))) return;
+                if (!warp_wait(bars.full(slot), phase, S.wait)) return;
+                uint32_t step_smem = ring + slot * stage_bytes;
+                for (uint32_t st = 0; st < spb; ++st, ++kb, step_smem += kBoxBytes) {
+                    if (fast_steps && kb * 8 + 8 <= kblk1)
+                        consume_step_full<NT, BOXES>(step_smem, box_stride, sc, p.nblk, kb, kblk0, ncols, xcur,
+                                                     L.xs_stride, fcur, L.fx_stride, acc, lane);
+                    else
+                        consume_step<NT, BOXES>(step_smem, box_stride, sc, p.nblk, kb, kblk0, kblk1, ncols, xcur,
+                                                L.xs_stride, fcur, L.fx_stride, acc, lane);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bars.empty(slot));
+            }
+        }
+        if (own) {
+            // All of K is in the registers: through this warp's own slot to
+            // the problem's epilogue.
+            const int g = lane >> 2, tig = lane & 3;
+#pragma unroll
+            for (int bx = 0; bx < BOXES; ++bx)
+#pragma unroll
+                for (int n = 0; n < NT; ++n) {
+                    float* Rb = red + (bx * 8 * NT + 8 * n + 2 * tig) * kRedStride;
+                    const float2 a01 = f32x2_unpack(acc[bx][n][0]), a23 = f32x2_unpack(acc[bx][n][1]);
+                    Rb[g] = a01.x;
+                    Rb[kRedStride + g] = a01.y;
+                    Rb[g + 8] = a23.x;
+                    Rb[kRedStride + g + 8] = a23.y;
+                }
+            __syncwarp();
+            P::epilogue(p, seq.u0 + static_cast<int>(uu), Sums<NT>{red, 1, kRedWarpFloats, kRedStride}, lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.sempty(ss));
+        }
+    }
+}
+
 // ------------------------------------------------------------------------
 // The kernel. P (the problem) supplies:
 //   static constexpr int NT, BOXES;
@@ -713,7 +1022,8 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
 //     tma3d = the tensor map is the 3D view (128 B, rows, K/256 segments) and one
 //     copy fetches a whole stage of a box; else it is the 2D view (K/2 B, rows).
 //     (stage() writes through StageDst and zeroes the factors of unused columns);
-//     cl = CTAs per cluster splitting K.
+//     cl = CTAs per cluster splitting K; layout.part_steps > 0 walks K in parts
+//     (lone CTAs of bulk-staged problems only).
 //   __device__ static int  num_units(const Params&);
 //   __device__ static int  chunk_of(const Params&, int u);
 //   __device__ static int  box_row(const Params&, int u, int box);      // TMA row coordinate
@@ -723,7 +1033,7 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
 //   __device__ static void stage(const Params&, int chunk, int kblk0, int kblk1, const StageDst&,
 //                                int tid, int nthreads);
 //   __device__ static void epilogue(const Params&, int u, const Sums<NT>&, int lane);
-template <class P>
+template <class P, bool kParts>
 __global__ void __launch_bounds__(Roles<P>::kThreads, 1)
     stream_kernel(const __grid_constant__ CUtensorMap tmap, const typename P::Params p) {
     extern __shared__ uint8_t smem_raw[];
@@ -758,9 +1068,10 @@ __global__ void __launch_bounds__(Roles<P>::kThreads, 1)
         const Bars& bars = S.bars;
         // Warps that own chunks of a unit: the arrivals its reduction buffer
         // and scale slot wait for (at least 1 so the count is valid; a rank
-        // with no K steps has no owners and never waits on them).
+        // with no K steps has no owners and never waits on them). K in parts:
+        // one owner per unit.
         const int cpu = (pl.kb1 - pl.kb0) / static_cast<int>(S.L.group);
-        const uint32_t nown = static_cast<uint32_t>(max(1, min(cpu, P::NCW)));
+        const uint32_t nown = kParts ? 1u : static_cast<uint32_t>(max(1, min(cpu, P::NCW)));
         for (uint32_t s = lane; s < S.L.nslot; s += 32) {
             mbar_init(bars.full(s), 1);
             mbar_init(bars.empty(s), S.L.steps / S.L.group);  // one arrival per consumer chunk of the stage
@@ -775,8 +1086,17 @@ __global__ void __launch_bounds__(Roles<P>::kThreads, 1)
             sts_u32_volatile(bars.red_tag(lane), lane - S.L.nrb);  // "unit lane - nrb" released it
             sts_u32_volatile(bars.red_count(lane), 0);
         }
-        if (lane < 2) mbar_init(bars.xbar(lane), P::NCW);  // staging
-        if (lane == 2) mbar_init(bars.xbar(2), 1);
+        if constexpr (kParts) {
+            if (lane < 2) {
+                mbar_init(bars.xbar(lane), 1);           // copy of buffer `lane` landed
+                mbar_init(bars.xbar(2 + lane), P::NCW);  // buffer `lane` converted
+                sts_u32_volatile(bars.xdone(lane), 0);
+                sts_u32_volatile(bars.xissued(lane), 0);
+            }
+        } else {
+            if (lane < 2) mbar_init(bars.xbar(lane), P::NCW);  // staging
+            if (lane == 2) mbar_init(bars.xbar(2), 1);
+        }
         if (lane == 4) *S.wait.abort = 0;
         fence_barrier_init();  // visible to the bulk-copy (async) proxy and to cluster peers
     }
@@ -789,27 +1109,63 @@ __global__ void __launch_bounds__(Roles<P>::kThreads, 1)
     pl.u0 = static_cast<int>((int64_t)U * group / ngroups);
     pl.u1 = static_cast<int>((int64_t)U * (group + 1) / ngroups);
 
-    if (warp == Roles<P>::kProducer)
-        producer_role<P>(p, S, pl, &tmap, lane);
-    else
-        consumer_role<P>(p, S, pl, warp, lane);
+    if constexpr (kParts) {
+        // K in parts (lone CTAs of bulk-staged problems; the launcher checks).
+        ItemSeq seq;
+        seq.u0 = pl.u0;
+        seq.nu = pl.u1 - pl.u0;
+        seq.ps = static_cast<int>(S.L.part_steps);
+        seq.nparts = (p.nkb + seq.ps - 1) / seq.ps;
+        seq.ub = static_cast<int>(S.L.ubatch);
+        seq.nkb = p.nkb;
+        seq.nblk = p.nblk;
+        seq.kb0 = pl.kb0;
+        seq.kb1 = pl.kb1;
+        seq.kblk0 = pl.kblk0;
+        seq.kblk1 = pl.kblk1;
+        if (warp == Roles<P>::kProducer)
+            producer_parts<P>(p, S, pl, seq, &tmap, lane);
+        else
+            consumer_parts<P>(p, S, seq, warp, lane);
+        __syncwarp();  // the producer's idle lanes wait for lane 0
+        // After a timeout a buffer's last copy may not have been waited for;
+        // let it land (bounded, whatever the abort flag says) before the CTA
+        // exits. At most one copy per buffer is outstanding.
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int never = 0;
+            const WaitCtx own{p.status, &never};
+            for (uint32_t b = 0; b < 2; ++b) {
+                const uint32_t n = lds_u32_volatile(S.bars.xissued(b));
+                if (n) mbar_wait(S.bars.xbar(b), (n - 1) & 1, own);
+            }
+        }
+    } else {
+        if (warp == Roles<P>::kProducer)
+            producer_role<P>(p, S, pl, &tmap, lane);
+        else
+            consumer_role<P>(p, S, pl, warp, lane);
 
-    // No CTA of a cluster leaves while another may still write to it.
-    if (pl.cl > 1) cluster_sync_all();
+        // No CTA of a cluster leaves while another may still write to it.
+        if (pl.cl > 1) cluster_sync_all();
+    }
 }
 
 // Host launcher: one CTA per SM (or clusters of p.cl CTAs), never more
 // groups than units.
-template <class Prob>
+// kParts = the layout walks K in parts (lone CTAs, p.cl == 1).
+template <class Prob, bool kParts = false>
 cudaError_t launch_stream_kernel(const CUtensorMap& tmap, const typename Prob::Params& p, int units, int num_sms,
                                  cudaStream_t stream) {
+    static_assert(!kParts || Prob::kBulkStage, "K in parts stages its activations by bulk copy");
+    if ((p.layout.part_steps != 0) != kParts || (kParts && p.cl > 1)) return cudaErrorInvalidValue;
     static int configured[64] = {0};  // dynamic smem already allowed, per device
     static int clusters_cached[64][9] = {};  // co-resident clusters per device and size
     const int smem = static_cast<int>(p.layout.total) + 1024;
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || configured[dev] < smem) {
-        cudaError_t e = cudaFuncSetAttribute(stream_kernel<Prob>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaError_t e = cudaFuncSetAttribute(stream_kernel<Prob, kParts>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = smem;
     }
@@ -835,7 +1191,7 @@ cudaError_t launch_stream_kernel(const CUtensorMap& tmap, const typename Prob::P
         cfg.gridDim = dim3(cl * (num_sms / cl));
         int nclusters = (dev >= 0 && dev < 64 && cl <= 8) ? clusters_cached[dev][cl] : 0;
         if (nclusters == 0) {
-            cudaError_t e = cudaOccupancyMaxActiveClusters(&nclusters, stream_kernel<Prob>, &cfg);
+            cudaError_t e = cudaOccupancyMaxActiveClusters(&nclusters, stream_kernel<Prob, kParts>, &cfg);
             if (e != cudaSuccess) return e;
             if (nclusters < 1) return cudaErrorInvalidConfiguration;
             if (dev >= 0 && dev < 64 && cl <= 8) clusters_cached[dev][cl] = nclusters;
@@ -845,7 +1201,7 @@ cudaError_t launch_stream_kernel(const CUtensorMap& tmap, const typename Prob::P
     if (groups > units) groups = units;
     if (groups < 1) groups = 1;
     cfg.gridDim = dim3(groups * cl);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, stream_kernel<Prob>, tmap, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, stream_kernel<Prob, kParts>, tmap, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

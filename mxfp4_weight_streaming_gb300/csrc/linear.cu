@@ -55,26 +55,62 @@ struct DenseProblem {
 
 static int tokens_to_nt(int T) { return T <= 8 ? 1 : (T <= 16 ? 2 : 4); }
 
-// few_units: at most 4 row groups per SM. Whole-stage chunks would then leave
-// most consumer warps idle, so stages are capped at 4 K steps (more, smaller
-// chunks); larger problems keep 7-8 step stages (larger copies, fewer
-// handshakes).
-static bool plan_linear_steps(int T, int K, int max_smem, int max_steps, int* cl, SmemLayout* L);
+// Plans, in order of preference:
+//  1. a lone CTA staging all of K (few_units: at most 4 row groups per SM;
+//     whole-stage chunks would then leave most consumer warps idle, so
+//     stages are capped at 4 K steps, more and smaller chunks; larger
+//     problems keep 7-8 step stages: larger copies, fewer handshakes),
+//     when the staged activations leave a ring of at least 64 KB;
+//  2. a lone CTA walking K in parts (the activations of all of K do not fit
+//     next to such a ring, e.g. T = 16 or 32 at K = 7168), if a CTA holds
+//     at least 2 units; else a lone CTA with a smaller ring;
+//  3. clusters of 2, 4 or 8 CTAs splitting K (preferred to parts when a CTA
+//     would hold a single unit, which parts would re-stage K for alone);
+//  4. K in parts whatever the units per CTA.
+static bool plan_linear_steps(int T, int K, int max_smem, int max_steps, int max_cl, int* cl, SmemLayout* L);
+static bool plan_linear_parts(int T, int K, int max_smem, int units_per_cta, SmemLayout* L);
 
-bool plan_linear(int T, int K, int max_smem, bool few_units, int* cl, SmemLayout* L) {
-    if (few_units && plan_linear_steps(T, K, max_smem, 4, cl, L)) return true;
-    return plan_linear_steps(T, K, max_smem, 8, cl, L);  // (also when the smaller stages fit no layout)
+bool plan_linear(int T, int K, int max_smem, bool few_units, int units_per_cta, int* cl, SmemLayout* L) {
+    SmemLayout lone{};
+    int lone_cl = 1;
+    const bool have_lone = (few_units && plan_linear_steps(T, K, max_smem, 4, 1, &lone_cl, &lone)) ||
+                           plan_linear_steps(T, K, max_smem, 8, 1, &lone_cl, &lone);
+    // Whole K per CTA, unless the staged activations leave a ring under
+    // 64 KB and parts are an option.
+    const bool lone_ring = lone.nslot * lone.steps * 2048u >= 64u * 1024u;
+    if (have_lone && (lone_ring || units_per_cta < 2)) {
+        *cl = 1;
+        *L = lone;
+        return true;
+    }
+    if (units_per_cta >= 2 && plan_linear_parts(T, K, max_smem, units_per_cta, L)) {
+        *cl = 1;
+        return true;
+    }
+    if (have_lone) {
+        *cl = 1;
+        *L = lone;
+        return true;
+    }
+    if (few_units && plan_linear_steps(T, K, max_smem, 4, 8, cl, L)) return true;
+    if (plan_linear_steps(T, K, max_smem, 8, 8, cl, L)) return true;  // (also when the smaller stages fit no layout)
+    *cl = 1;
+    return plan_linear_parts(T, K, max_smem, units_per_cta, L);  // last resort for one unit per CTA
 }
 
-static bool plan_linear_steps(int T, int K, int max_smem, int max_steps, int* cl, SmemLayout* L) {
+static int dense_ncw(int nt) {
+    return nt == 1 ? DenseProblem<1>::NCW : (nt == 2 ? DenseProblem<2>::NCW : DenseProblem<4>::NCW);
+}
+
+static bool plan_linear_steps(int T, int K, int max_smem, int max_steps, int max_cl, int* cl, SmemLayout* L) {
     const int nblk = K / 32;
     const int nkb = (K + 255) / 256;
-    for (int c = 1; c <= 8; c *= 2) {
+    for (int c = 1; c <= max_cl; c *= 2) {
         if (c > 1 && c > nkb) break;
         const int nkb_c = (nkb + c - 1) / c;
         const int nb_local = nkb_c * 8 < nblk ? nkb_c * 8 : nblk;
         const int nt = tokens_to_nt(T);
-        const int ncw = nt == 1 ? DenseProblem<1>::NCW : (nt == 2 ? DenseProblem<2>::NCW : DenseProblem<4>::NCW);
+        const int ncw = dense_ncw(nt);
         // The stage size must divide the K steps of every rank (the same split
         // the kernel uses: rank r takes [min(nkb, r*nkb_c), min(nkb, +nkb_c))).
         int g = 0;  // gcd of the ranks' step counts (a rank with none adds nothing)
@@ -98,11 +134,54 @@ static bool plan_linear_steps(int T, int K, int max_smem, int max_steps, int* cl
     return false;
 }
 
+// K in parts: the part (a divisor of the K steps) is the largest whose two
+// activation buffers take at most 72 KB; units go in batches of one per
+// consumer warp at most (the CTA's share when it fits, halved until the ring
+// keeps 64 KB). A stage holds up to 4 K steps of one unit.
+static bool plan_linear_parts(int T, int K, int max_smem, int units_per_cta, SmemLayout* L) {
+    const int nblk = K / 32;
+    const int nkb = (K + 255) / 256;
+    const int nt = tokens_to_nt(T);
+    const int ncw = dense_ncw(nt);
+    int ub_max = units_per_cta < ncw ? units_per_cta : ncw;
+    ub_max = ub_max < 16 ? ub_max : 16;
+    // First pass: only parts that allow stages of at least 2 steps.
+    for (int pass = 0; pass < 2; ++pass) {
+        for (int ps = nkb; ps >= 1; --ps) {
+            if (nkb % ps != 0) continue;
+            if (pass == 0 && ps % 2 != 0 && ps % 3 != 0) continue;
+            const int pblk = ps * 8 < nblk ? ps * 8 : nblk;
+            if (ps > 1 && 2L * T * (pblk * 64 + 16) > 72L * 1024) continue;
+            int spb = 1;
+            for (int sb = ps < 4 ? ps : 4; sb >= 1; --sb)
+                if (ps % sb == 0) {
+                    spb = sb;
+                    break;
+                }
+            for (int ub = ub_max; ub >= 1; ub = ub > 1 ? ub / 2 : 0) {
+                // A larger batch re-stages the activations less often, but
+                // its scale slots must leave a ring of at least 64 KB.
+                if (plan_layout(nt, 1, pblk, nblk, T, 1, ncw, kRedStride, spb, spb, ps, max_smem, L, ps, ub) &&
+                    (ub == 1 || L->nslot * L->steps * 2048u >= 64u * 1024u))
+                    return true;
+            }
+        }
+    }
+    return false;
+}
+
 cudaError_t launch_linear(const CUtensorMap& tmap, const LinearParams& p, int num_sms, cudaStream_t stream) {
+    const bool parts = p.layout.part_steps != 0;
     switch (tokens_to_nt(p.T)) {
-        case 1: return launch_stream_kernel<DenseProblem<1>>(tmap, p, p.n_rg, num_sms, stream);
-        case 2: return launch_stream_kernel<DenseProblem<2>>(tmap, p, p.n_rg, num_sms, stream);
-        default: return launch_stream_kernel<DenseProblem<4>>(tmap, p, p.n_rg, num_sms, stream);
+        case 1:
+            return parts ? launch_stream_kernel<DenseProblem<1>, true>(tmap, p, p.n_rg, num_sms, stream)
+                         : launch_stream_kernel<DenseProblem<1>>(tmap, p, p.n_rg, num_sms, stream);
+        case 2:
+            return parts ? launch_stream_kernel<DenseProblem<2>, true>(tmap, p, p.n_rg, num_sms, stream)
+                         : launch_stream_kernel<DenseProblem<2>>(tmap, p, p.n_rg, num_sms, stream);
+        default:
+            return parts ? launch_stream_kernel<DenseProblem<4>, true>(tmap, p, p.n_rg, num_sms, stream)
+                         : launch_stream_kernel<DenseProblem<4>>(tmap, p, p.n_rg, num_sms, stream);
     }
 }
 

@@ -26,8 +26,9 @@ struct LinearParams {
 };
 
 // Chooses the cluster size (1, 2, 4 or 8 CTAs splitting K) and the shared
-// memory plan; false if no plan fits.
-bool plan_linear(int T, int K, int max_smem, bool few_units, int* cl, SmemLayout* L);
+// memory plan (whole K per CTA, or K in parts); false if no plan fits.
+// units_per_cta = row groups per CTA of the launch (ceil(n_rg / CTAs)).
+bool plan_linear(int T, int K, int max_smem, bool few_units, int units_per_cta, int* cl, SmemLayout* L);
 cudaError_t launch_linear(const CUtensorMap& tmap, const LinearParams& p, int num_sms, cudaStream_t stream);
 cudaError_t launch_quantize(const float* w, int64_t n, int64_t k, uint8_t* wq, uint8_t* ws, cudaStream_t stream,
                             int num_sms);

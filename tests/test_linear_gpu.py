@@ -80,6 +80,45 @@ def test_linear_cluster_split_k(t, k, n):
     assert mx.last_device_status() == mx.MXFP4_OK
 
 
+@pytest.mark.parametrize("t,k,n", [(16, 7168, 4900), (32, 7200, 4900), (12, 7168, 4864), (17, 4096, 5000),
+                                   (24, 14336, 4900)])
+def test_linear_k_parts(t, k, n):
+    """Token counts whose activations over all of K leave no useful ring in
+    one SM, with at least 2 row groups per CTA: each CTA walks K in parts
+    (double-buffered activation parts; each row group's sums stay with one
+    warp across the parts). Covers a ragged row group, K % 256 != 0 (29
+    one-step parts, the last one block long), partial token tiles (12 of 16,
+    17 of 32) and CTAs with fewer row groups than warps."""
+    mx = lib()
+    w, x = linear_case(80 + t, t, k, n)
+    wq, ws, rq, rs = _pack_both(w)
+    y = mx.linear(x, wq, ws)
+    torch.cuda.synchronize()
+    y_ref, rss = oracle.linear(x, rq, rs)
+    assert_within(bf16_to_f64(y), y_ref, rss, f"k parts t={t} k={k} n={n}")
+    assert mx.last_device_status() == mx.MXFP4_OK
+
+
+def test_linear_k_parts_many_batches_sampled():
+    """T=32, K=4096, N=40008: 16-17 row groups per CTA in batches of 8 (one
+    per consumer warp), so every CTA re-stages the activation parts per
+    batch and a CTA with 17 ends on a one-unit batch; sampled rows
+    (including the ragged last group of 8) against the oracle."""
+    mx = lib()
+    t, k, n = 32, 4096, 40008
+    w, x = linear_case(90, t, k, n)
+    wq, ws = mx.quantize(w)
+    y = mx.linear(x, wq, ws)
+    torch.cuda.synchronize()
+    rows = np.union1d(sample_rows(n, 256, seed=90), np.arange(n - 16, n))
+    rows_t = torch.from_numpy(rows).cuda()
+    rq, rs = oracle.quantize(w[rows_t].cpu().numpy())
+    del w
+    y_ref, rss = oracle.linear(x, rq, rs)
+    assert_within(bf16_to_f64(y[:, rows_t]), y_ref, rss, "k parts, many batches")
+    assert mx.last_device_status() == mx.MXFP4_OK
+
+
 def test_linear_config1_full():
     """T=1, K=N=1024, seed 0: whole output against the oracle."""
     mx = lib()

@@ -79,6 +79,15 @@ struct Bars {
     __device__ uint32_t xissued(uint32_t b) const { return tags + 4 * (nslot + nss + 2 * nrb + 2 + b); }
 };
 
+// Next position of a ring of n slots: slot index and the parity of its
+// current round (no division on the per-unit path).
+__device__ __forceinline__ void ring_next(uint32_t& i, uint32_t& phase, uint32_t n) {
+    if (++i == n) {
+        i = 0;
+        phase ^= 1u;
+    }
+}
+
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx& w) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, w));
 }
@@ -143,10 +152,22 @@ __device__ __forceinline__ void stage_bf16_block(const uint32_t (&w)[16], uint8_
     if (amax != 0) c = staging_exponent(floor_log2_f32_bits(amax << 16));
     const Pow2Scaler sc(c);
     uint32_t o[16];
+    if (!sc.two) {
+        // One packed multiply per pair of values (the usual case).
+        const uint64_t s2 = f32x2_pack(sc.s1, sc.s1);
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        __half2 h = __floats2half2_rn(sc(__uint_as_float(w[j] << 16)), sc(__uint_as_float(w[j] & 0xffff0000u)));
-        o[j] = *reinterpret_cast<uint32_t*>(&h);
+        for (int j = 0; j < 16; ++j) {
+            const float2 v = f32x2_unpack(
+                f32x2_mul(f32x2_pack(__uint_as_float(w[j] << 16), __uint_as_float(w[j] & 0xffff0000u)), s2));
+            __half2 h = __floats2half2_rn(v.x, v.y);
+            o[j] = *reinterpret_cast<uint32_t*>(&h);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            __half2 h = __floats2half2_rn(sc(__uint_as_float(w[j] << 16)), sc(__uint_as_float(w[j] & 0xffff0000u)));
+            o[j] = *reinterpret_cast<uint32_t*>(&h);
+        }
     }
     const uint32_t d = smem_addr(dst);
 #pragma unroll
@@ -220,9 +241,10 @@ __device__ __forceinline__ void convert_columns(int ncol, int nb, const StageDst
     // column stride puts them 4 banks apart, so a warp's 16-byte accesses
     // need 4 wavefronts for T >= 4 (consecutive blocks of one column, 64
     // bytes apart, would need 16).
+    // Item it = b * ncol + t, advanced by nthreads without a division.
+    const int db = nthreads / ncol, dt = nthreads - db * ncol;
+    int b = tid / ncol, t = tid - (tid / ncol) * ncol;
     for (int it = tid; it < ncol * nb; it += nthreads) {
-        const int b = it / ncol;
-        const int t = it - b * ncol;
         const uint32_t a = xs_s + t * dst.xs_stride + b * 64;
         uint32_t w[16];
 #pragma unroll
@@ -234,10 +256,26 @@ __device__ __forceinline__ void convert_columns(int ncol, int nb, const StageDst
             w[4 * q + 3] = v.w;
         }
         stage_bf16_block(w, dst.col(t, b), dst.factor(t, b));
+        t += dt;
+        b += db;
+        if (t >= ncol) {
+            t -= ncol;
+            ++b;
+        }
     }
-    for (int it = tid; it < nb * (kCols - ncol); it += nthreads) {
-        const int b = it / (kCols - ncol);
-        *dst.factor(ncol + (it - b * (kCols - ncol)), b) = 0.0f;
+    const int nz = kCols - ncol;
+    if (nz > 0) {
+        const int zb = nthreads / nz, zt = nthreads - zb * nz;
+        int bz = tid / nz, tz = tid - (tid / nz) * nz;
+        for (int it = tid; it < nb * nz; it += nthreads) {
+            *dst.factor(ncol + tz, bz) = 0.0f;
+            tz += zt;
+            bz += zb;
+            if (tz >= nz) {
+                tz -= nz;
+                ++bz;
+            }
+        }
     }
 }
 
@@ -591,14 +629,15 @@ __device__ void producer_parts(const typename P::Params& p, const Smem& S, const
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
     bool ok = true;
     uint32_t staged = 0, sissued = 0;
+    uint32_t slot = 0, rph = 0;  // ring slot of stage `staged` and its round parity
+    uint32_t ss = 0, sph = 0;    // scale slot of the next unit's first part and its round parity
     const int ni = seq.count();
     for (int v = 0; v < ni && ok; ++v) {
         const Item it = seq.at(v);
         const int u = it.u;
         const uint32_t uu = it.uu;
         if (it.part == 0) {
-            const uint32_t ss = uu % L.nss;
-            if (!mbar_wait(bars.sempty(ss), ((uu / L.nss) & 1) ^ 1, S.wait)) {
+            if (!mbar_wait(bars.sempty(ss), sph ^ 1, S.wait)) {
                 ok = false;
                 break;
             }
@@ -621,13 +660,13 @@ __device__ void producer_parts(const typename P::Params& p, const Smem& S, const
                     bulk_load(dst + bx * scale_bytes, P::scale_src(p, u, bx), bulk, bars.sfull(ss), policy);
             }
             ++sissued;
+            ring_next(ss, sph, L.nss);
         }
         int rows[BOXES];
 #pragma unroll
         for (int bx = 0; bx < BOXES; ++bx) rows[bx] = P::box_row(p, u, bx);
         for (int kb = it.kb0; kb < it.kb1; kb += static_cast<int>(spb)) {
-            const uint32_t slot = staged % L.nslot;
-            if (!mbar_wait(bars.empty(slot), ((staged / L.nslot) & 1) ^ 1, S.wait)) {
+            if (!mbar_wait(bars.empty(slot), rph ^ 1, S.wait)) {
                 ok = false;
                 break;
             }
@@ -652,6 +691,7 @@ __device__ void producer_parts(const typename P::Params& p, const Smem& S, const
                 }
             }
             ++staged;
+            ring_next(slot, rph, L.nslot);
         }
     }
     if (!ok) {
@@ -721,7 +761,9 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
     uint32_t stage = c / cps;
     uint32_t slot = stage % L.nslot;
     uint32_t phase = (stage / L.nslot) & 1u;
-    for (int u = pl.u0; u < pl.u1; ++u) {
+    uint32_t ss = 0, sph = 0;  // scale slot of unit uu and its round parity
+    uint32_t rb = 0, rph = 0;  // reduction buffer of unit uu (uu % nrb)
+    for (int u = pl.u0; u < pl.u1; ++u, ring_next(ss, sph, L.nss), ring_next(rb, rph, L.nrb)) {
         const uint32_t uu = u - pl.u0;
         const int chunk = P::chunk_of(p, u);
         if (cur_chunk < 0) pdl_wait_previous();  // activations may come from the previous kernel
@@ -747,7 +789,6 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
             cur_chunk = chunk;
             ncols = P::ncols(p, chunk);
         }
-        const uint32_t ss = uu % L.nss;
         const uint32_t cb = uu * cpu;  // first chunk of this unit
         // A warp owns chunks of this unit iff its next chunk lies inside it;
         // its partial goes to slot c - cb (< NCW, since its previous chunk
@@ -765,7 +806,7 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
             // This warp may be several units ahead of the scale ring: the tag
             // says the slot holds this unit's scales (or is being filled).
             if (!__all_sync(0xffffffffu, wait_shared_value(bars.scale_tag(ss), uu, S.wait))) return;
-            if (!warp_wait(bars.sfull(ss), (uu / L.nss) & 1, S.wait)) return;
+            if (!warp_wait(bars.sfull(ss), sph, S.wait)) return;
             const uint32_t sc = scb + ss * L.ss_bytes;
             for (; c < cb + cpu; c += P::NCW) {
                 // A warp may run several stages ahead of the ring: first wait
@@ -803,7 +844,6 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
         }
         // Reduction buffer uu % nrb (on rank 0) is free once unit uu - nrb is
         // finished; its finisher tags the buffer on every rank.
-        const uint32_t rb = uu % L.nrb;
         if (!__all_sync(0xffffffffu, wait_shared_value(bars.red_tag(rb), uu - L.nrb, S.wait))) return;
         if (lone)
             __threadfence_block();

@@ -68,8 +68,9 @@ def test_linear_many_tokens(t):
 @pytest.mark.parametrize("t,k,n", [(16, 7168, 130), (32, 7168, 70), (24, 14336, 40), (8, 16384, 33),
                                    (12, 30720, 17)])
 def test_linear_cluster_split_k(t, k, n):
-    """Token counts whose staged activations exceed one SM: K is split over a
-    thread-block cluster and the partial sums meet through DSMEM."""
+    """Token counts whose staged activations exceed one SM, with one row group
+    per CTA: K is split over a thread-block cluster and the partial sums meet
+    through DSMEM."""
     mx = lib()
     w, x = linear_case(60 + t, t, k, n)
     wq, ws, rq, rs = _pack_both(w)

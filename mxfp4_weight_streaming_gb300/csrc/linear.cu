@@ -67,14 +67,15 @@ static int tokens_to_nt(int T) { return T <= 8 ? 1 : (T <= 16 ? 2 : 4); }
 //  3. clusters of 2, 4 or 8 CTAs splitting K (preferred to parts when a CTA
 //     would hold a single unit, which parts would re-stage K for alone);
 //  4. K in parts whatever the units per CTA.
-static bool plan_linear_steps(int T, int K, int max_smem, int max_steps, int max_cl, int* cl, SmemLayout* L);
+static bool plan_linear_steps(int T, int K, int max_smem, int max_steps, int max_cl, int units_per_cta, int* cl,
+                              SmemLayout* L);
 static bool plan_linear_parts(int T, int K, int max_smem, int units_per_cta, SmemLayout* L);
 
 bool plan_linear(int T, int K, int max_smem, bool few_units, int units_per_cta, int* cl, SmemLayout* L) {
     SmemLayout lone{};
     int lone_cl = 1;
-    const bool have_lone = (few_units && plan_linear_steps(T, K, max_smem, 4, 1, &lone_cl, &lone)) ||
-                           plan_linear_steps(T, K, max_smem, 8, 1, &lone_cl, &lone);
+    const bool have_lone = (few_units && plan_linear_steps(T, K, max_smem, 4, 1, units_per_cta, &lone_cl, &lone)) ||
+                           plan_linear_steps(T, K, max_smem, 8, 1, units_per_cta, &lone_cl, &lone);
     // Whole K per CTA, unless the staged activations leave a ring under
     // 64 KB and parts are an option.
     const bool lone_ring = lone.nslot * lone.steps * 2048u >= 64u * 1024u;
@@ -92,8 +93,8 @@ bool plan_linear(int T, int K, int max_smem, bool few_units, int units_per_cta, 
         *L = lone;
         return true;
     }
-    if (few_units && plan_linear_steps(T, K, max_smem, 4, 8, cl, L)) return true;
-    if (plan_linear_steps(T, K, max_smem, 8, 8, cl, L)) return true;  // (also when the smaller stages fit no layout)
+    if (few_units && plan_linear_steps(T, K, max_smem, 4, 8, units_per_cta, cl, L)) return true;
+    if (plan_linear_steps(T, K, max_smem, 8, 8, units_per_cta, cl, L)) return true;  // (also when the smaller stages fit no layout)
     *cl = 1;
     return plan_linear_parts(T, K, max_smem, units_per_cta, L);  // last resort for one unit per CTA
 }
@@ -102,7 +103,8 @@ static int dense_ncw(int nt) {
     return nt == 1 ? DenseProblem<1>::NCW : (nt == 2 ? DenseProblem<2>::NCW : DenseProblem<4>::NCW);
 }
 
-static bool plan_linear_steps(int T, int K, int max_smem, int max_steps, int max_cl, int* cl, SmemLayout* L) {
+static bool plan_linear_steps(int T, int K, int max_smem, int max_steps, int max_cl, int units_per_cta, int* cl,
+                              SmemLayout* L) {
     const int nblk = K / 32;
     const int nkb = (K + 255) / 256;
     for (int c = 1; c <= max_cl; c *= 2) {
@@ -126,7 +128,17 @@ static bool plan_linear_steps(int T, int K, int max_smem, int max_steps, int max
             g = a;
         }
         const int steps = stage_steps(1, g, 0, max_steps);
-        if (plan_layout(nt, 1, nb_local, nblk, T, c, ncw, kRedStride, steps, steps, nkb_c, max_smem, L)) {
+        // Consumer chunk: a whole stage, unless a lone CTA then has fewer
+        // chunks than consumer warps (e.g. one row group of 4 steps); then the
+        // largest divisor of the stage that gives every warp a chunk, or 1.
+        int grp = steps;
+        if (c == 1)
+            while (grp > 1 && units_per_cta * (nkb / grp) < ncw) {
+                int d = grp - 1;
+                while (steps % d != 0) --d;
+                grp = d;
+            }
+        if (plan_layout(nt, 1, nb_local, nblk, T, c, ncw, kRedStride, steps, grp, nkb_c, max_smem, L)) {
             *cl = c;
             return true;
         }

@@ -91,6 +91,35 @@ int mxfp4_linear(const void* x, int64_t t, int64_t k, const uint8_t* wq, const u
                  void* y, void* stream);
 
 /*
+ * How mxfp4_linear cuts the weight stream for one shape (the plan it would
+ * launch). The pages have no counterpart to this entry point: it reports
+ * the kernel's choices, which set its speed, and lets them be checked
+ * without a GPU.
+ *   t, k, n    as for mxfp4_linear (same argument checks)
+ *   num_sms    streaming multiprocessors of the device
+ *              (cudaDevAttrMultiProcessorCount; 152 on GB300)
+ *   max_smem   opt-in shared memory per block in bytes
+ *              (cudaDevAttrMaxSharedMemoryPerBlockOptin)
+ *   out        host struct, written on MXFP4_OK (caller-owned)
+ * Host only: no CUDA call, no device needed. Returns MXFP4_ERR_SHAPE when
+ * mxfp4_linear would (no plan fits max_smem).
+ */
+typedef struct {
+    int32_t mode;        /* 0: whole K per CTA; 1: K walked in parts per CTA;
+                            2: K split over a thread-block cluster */
+    int32_t ctas;        /* CTAs launched (mode 2: an upper bound; the number
+                            of co-resident clusters decides) */
+    int32_t cluster;     /* CTAs per cluster (1 unless mode 2) */
+    int32_t stage_steps; /* K steps of 256 values per weight-ring stage */
+    int32_t chunk_steps; /* K steps a consumer warp takes at a time */
+    int32_t ring_slots;  /* stages in the weight ring */
+    int32_t part_steps;  /* mode 1: K steps per part; else 0 */
+    int32_t batch_units; /* mode 1: row groups of 16 rows per batch; else 0 */
+    int32_t smem_bytes;  /* dynamic shared memory per CTA */
+} mxfp4_linear_plan_t;
+int mxfp4_linear_plan(int64_t t, int64_t k, int64_t n, int num_sms, int max_smem, mxfp4_linear_plan_t* out);
+
+/*
  * Bytes of device workspace mxfp4_moe needs for t tokens, e experts,
  * top_k experts per token, hidden size `hidden` and expert width `inter`.
  */

@@ -6,8 +6,9 @@ is no CPU path: if the library has not been built, importing the C entry
 points raises, and every compute call needs a CUDA device.
 
 C entry points (same names as the header): mxfp4_quantize, mxfp4_linear,
-mxfp4_moe, mxfp4_moe_workspace_size, mxfp4_last_device_status,
-mxfp4_strerror. Convenience wrappers: quantize, linear, moe.
+mxfp4_linear_plan, mxfp4_moe, mxfp4_moe_workspace_size,
+mxfp4_last_device_status, mxfp4_strerror. Convenience wrappers: quantize,
+linear, linear_plan (host only), moe.
 """
 from __future__ import annotations
 
@@ -25,8 +26,8 @@ MXFP4_ERR_WORKSPACE = 4
 MXFP4_ERR_CUDA = 5
 MXFP4_ERR_TIMEOUT = 6
 
-EXPORTED = ["mxfp4_strerror", "mxfp4_quantize", "mxfp4_linear", "mxfp4_moe_workspace_size", "mxfp4_moe",
-            "mxfp4_last_device_status"]
+EXPORTED = ["mxfp4_strerror", "mxfp4_quantize", "mxfp4_linear", "mxfp4_linear_plan", "mxfp4_moe_workspace_size",
+            "mxfp4_moe", "mxfp4_last_device_status"]
 
 _lib = None
 
@@ -35,6 +36,15 @@ class Mxfp4Error(RuntimeError):
     def __init__(self, status: int, what: str):
         super().__init__(f"{what}: {strerror(status)}")
         self.status = status
+
+
+class LinearPlan(ctypes.Structure):
+    """mxfp4_linear_plan_t: how mxfp4_linear cuts the weight stream."""
+    _fields_ = [(name, ctypes.c_int32) for name in ("mode", "ctas", "cluster", "stage_steps", "chunk_steps",
+                                                     "ring_slots", "part_steps", "batch_units", "smem_bytes")]
+
+
+PLAN_MODES = {0: "whole K", 1: "K in parts", 2: "cluster split of K"}
 
 
 def load() -> ctypes.CDLL:
@@ -58,6 +68,8 @@ def load() -> ctypes.CDLL:
     L.mxfp4_moe.argtypes = [P, I64, I64, P, I64, I, P, P, P, P, I64, P, P, P, P, ctypes.c_size_t, P]
     L.mxfp4_last_device_status.restype = I
     L.mxfp4_last_device_status.argtypes = [P]
+    L.mxfp4_linear_plan.restype = I
+    L.mxfp4_linear_plan.argtypes = [I64, I64, I64, I, I, ctypes.POINTER(LinearPlan)]
     _lib = L
     return L
 
@@ -150,6 +162,15 @@ def moe(x, logits, top_k, w1q, w1s, w2q, w2s, workspace=None, out=None, topk_ids
                      w2q.data_ptr(), w2s.data_ptr(), inter, y.data_ptr(), ids_ptr, gw_ptr, workspace.data_ptr(),
                      workspace.numel(), _stream(stream)), "mxfp4_moe")
     return y
+
+
+def linear_plan(t, k, n, num_sms=152, max_smem=232448) -> dict:
+    """The plan mxfp4_linear uses for this shape on a device with num_sms SMs
+    and max_smem bytes of opt-in shared memory per block (GB300 defaults).
+    Host only; raises Mxfp4Error when no plan fits."""
+    plan = LinearPlan()
+    _check(load().mxfp4_linear_plan(t, k, n, num_sms, max_smem, ctypes.byref(plan)), "mxfp4_linear_plan")
+    return {name: getattr(plan, name) for name, _ in LinearPlan._fields_}
 
 
 def last_device_status(stream=None) -> int:

@@ -117,6 +117,24 @@ constexpr int kPlanCache = 16;
 thread_local LinearPlan t_plans[kPlanCache];
 thread_local int t_plan_next = 0;
 
+// The launch plan of a linear call (host only): cluster size and shared
+// memory layout for t tokens, k, n on a device with num_sms SMs and max_smem
+// bytes of opt-in shared memory per block. False if no plan fits.
+bool linear_plan(int64_t t, int64_t k, int64_t n, int num_sms, int max_smem, int* cl, mxfp4::SmemLayout* L) {
+    const int64_t n_rg = (n + 15) / 16;
+    const bool few_units = n_rg <= 4 * static_cast<int64_t>(num_sms);
+    const int64_t ctas = n_rg < num_sms ? n_rg : num_sms;
+    const int units_per_cta = static_cast<int>((n_rg + ctas - 1) / ctas);
+    return mxfp4::plan_linear(static_cast<int>(t), static_cast<int>(k), max_smem, few_units, units_per_cta, cl, L);
+}
+
+// Argument checks shared by mxfp4_linear and mxfp4_linear_plan.
+int linear_shape_status(int64_t t, int64_t k, int64_t n) {
+    if (t <= 0 || k <= 0 || n <= 0) return MXFP4_ERR_INVALID_ARG;
+    if (k % 32 != 0 || t > 32 || n >= (int64_t(1) << 31) || k >= (int64_t(1) << 31)) return MXFP4_ERR_SHAPE;
+    return MXFP4_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -146,8 +164,8 @@ int mxfp4_quantize(const float* w, int64_t n, int64_t k, uint8_t* wq, uint8_t* w
 
 int mxfp4_linear(const void* x, int64_t t, int64_t k, const uint8_t* wq, const uint8_t* ws, int64_t n, void* y,
                  void* stream) {
-    if (!x || !wq || !ws || !y || t <= 0 || k <= 0 || n <= 0) return MXFP4_ERR_INVALID_ARG;
-    if (k % 32 != 0 || t > 32 || n >= (int64_t(1) << 31) || k >= (int64_t(1) << 31)) return MXFP4_ERR_SHAPE;
+    if (!x || !wq || !ws || !y) return MXFP4_ERR_INVALID_ARG;
+    if (int rc = linear_shape_status(t, k, n)) return rc;
     if (!aligned(x, 16) || !aligned(wq, 16) || !aligned(ws, 16) || !aligned(y, 2)) return MXFP4_ERR_ALIGN;
     DeviceInfo* d = nullptr;
     if (int rc = device_info(&d)) return rc;
@@ -161,13 +179,7 @@ int mxfp4_linear(const void* x, int64_t t, int64_t k, const uint8_t* wq, const u
         }
     if (!plan) {
         LinearPlan fresh;
-        const int64_t n_rg = (n + 15) / 16;
-        const bool few_units = n_rg <= 4 * static_cast<int64_t>(d->num_sms);
-        const int64_t ctas = n_rg < d->num_sms ? n_rg : d->num_sms;
-        const int units_per_cta = static_cast<int>((n_rg + ctas - 1) / ctas);
-        if (!mxfp4::plan_linear(static_cast<int>(t), static_cast<int>(k), d->max_smem, few_units, units_per_cta,
-                                &fresh.p.cl, &fresh.p.layout))
-            return MXFP4_ERR_SHAPE;
+        if (!linear_plan(t, k, n, d->num_sms, d->max_smem, &fresh.p.cl, &fresh.p.layout)) return MXFP4_ERR_SHAPE;
         if (int rc = encode_weight_map(&fresh.map, wq, n, k, static_cast<int>(fresh.p.layout.steps), &fresh.p.tma3d))
             return rc;
         fresh.dev = dev;
@@ -194,6 +206,30 @@ int mxfp4_linear(const void* x, int64_t t, int64_t k, const uint8_t* wq, const u
     p.n_rg = static_cast<int>((n + 15) / 16);
     cudaError_t e = mxfp4::launch_linear(map, p, d->num_sms, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
+}
+
+int mxfp4_linear_plan(int64_t t, int64_t k, int64_t n, int num_sms, int max_smem, mxfp4_linear_plan_t* out) {
+    if (!out || num_sms <= 0 || max_smem <= 0) return MXFP4_ERR_INVALID_ARG;
+    if (int rc = linear_shape_status(t, k, n)) return rc;
+    int cl = 1;
+    mxfp4::SmemLayout L{};
+    if (!linear_plan(t, k, n, num_sms, max_smem, &cl, &L)) return MXFP4_ERR_SHAPE;
+    const int64_t n_rg = (n + 15) / 16;
+    mxfp4_linear_plan_t r{};
+    r.mode = L.part_steps ? 1 : (cl > 1 ? 2 : 0);
+    r.cluster = cl;
+    // CTAs: one per SM, never more groups than row groups; for clusters the
+    // co-resident cluster count at launch may be lower than this bound.
+    const int64_t groups = cl > 1 ? num_sms / cl : num_sms;
+    r.ctas = static_cast<int32_t>(cl * (groups < n_rg ? groups : n_rg));
+    r.stage_steps = static_cast<int32_t>(L.steps);
+    r.chunk_steps = static_cast<int32_t>(L.group);
+    r.ring_slots = static_cast<int32_t>(L.nslot);
+    r.part_steps = static_cast<int32_t>(L.part_steps);
+    r.batch_units = static_cast<int32_t>(L.ubatch);
+    r.smem_bytes = static_cast<int32_t>(L.total) + 1024;  // + alignment slack, as launched
+    *out = r;
+    return MXFP4_OK;
 }
 
 size_t mxfp4_moe_workspace_size(int64_t t, int64_t e, int top_k, int64_t hidden, int64_t inter) {

@@ -1,0 +1,116 @@
+"""The launch plans of mxfp4_linear, checked on the host (no GPU): the choice
+between whole K per CTA, K walked in parts and a cluster split of K, and the
+invariants every plan must keep for the kernel's indexing to hold."""
+import math
+
+import pytest
+
+import mxfp4_weight_streaming_gb300 as mx
+
+SMS, SMEM = 152, 232448  # GB300: SMs and opt-in shared memory per block
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    from mxfp4_weight_streaming_gb300 import build
+    build.build()
+    mx.load()
+
+
+def consumer_warps(t):
+    return 14 if t <= 8 else (12 if t <= 16 else 8)
+
+
+@pytest.mark.parametrize("t,k,n,mode,stage,chunk,part,batch", [
+    (4, 7168, 7168, 0, 4, 4, 0, 0),      # verify: 3 row groups per CTA, 4-step stages and chunks
+    (1, 1024, 1024, 0, 4, 1, 0, 0),      # one row group of 4 steps per CTA: 1-step chunks
+    (1, 7168, 18432, 0, 7, 7, 0, 0),     # FFN up, whole-stage chunks
+    (8, 7168, 18432, 0, 7, 7, 0, 0),
+    (4, 7168, 129280, 0, 7, 7, 0, 0),    # LM head
+    (16, 7168, 18432, 1, 4, 4, 4, 8),    # activations of all of K fill shared memory: K in parts
+    (32, 7168, 18432, 1, 2, 2, 2, 8),
+    (32, 7200, 4900, 1, 1, 1, 1, 3),     # 29 K steps (prime): one-step parts
+])
+def test_plan_choices(t, k, n, mode, stage, chunk, part, batch):
+    p = mx.linear_plan(t, k, n, SMS, SMEM)
+    assert (p["mode"], p["stage_steps"], p["chunk_steps"], p["part_steps"], p["batch_units"]) == \
+        (mode, stage, chunk, part, batch), p
+    assert p["cluster"] == 1 and p["ctas"] == min(SMS, (n + 15) // 16)
+
+
+def test_cluster_only_for_single_row_group_ctas():
+    p = mx.linear_plan(16, 7168, 130, SMS, SMEM)
+    assert p["mode"] == 2 and p["cluster"] == 2 and p["ctas"] == 2 * 9
+    p = mx.linear_plan(16, 7168, 4900, SMS, SMEM)  # 2-3 row groups per CTA
+    assert p["mode"] == 1
+
+
+def grid():
+    for t in (1, 2, 3, 4, 5, 8, 9, 12, 16, 17, 23, 24, 32):
+        for k in (32, 96, 1024, 1056, 2048, 4096, 7168, 7200, 14336, 16384):
+            for n in (1, 17, 130, 1024, 4900, 18432, 129280):
+                yield t, k, n
+
+
+def test_plan_invariants_over_shapes():
+    seen = set()
+    for t, k, n in grid():
+        try:
+            p = mx.linear_plan(t, k, n, SMS, SMEM)
+        except mx.Mxfp4Error as e:
+            assert e.status == mx.MXFP4_ERR_SHAPE
+            continue
+        seen.add(p["mode"])
+        nkb = -(-k // 256)
+        n_rg = -(-n // 16)
+        upc = -(-n_rg // min(SMS, n_rg))
+        ncw = consumer_warps(t)
+        where = f"t={t} k={k} n={n}: {p}"
+        assert p["smem_bytes"] <= SMEM, where
+        assert p["stage_steps"] >= 1 and p["stage_steps"] % p["chunk_steps"] == 0, where
+        assert p["ring_slots"] >= 2, where
+        if p["mode"] == 0:
+            assert p["cluster"] == 1 and p["ctas"] == min(SMS, n_rg), where
+            assert nkb % p["stage_steps"] == 0, where
+            # whole-stage chunks unless some warp would get none
+            if p["chunk_steps"] < p["stage_steps"]:
+                bigger = [g for g in range(p["chunk_steps"] + 1, p["stage_steps"] + 1) if p["stage_steps"] % g == 0]
+                assert all(upc * (nkb // g) < ncw for g in bigger), where
+        elif p["mode"] == 1:
+            assert p["cluster"] == 1 and p["ctas"] == min(SMS, n_rg), where
+            assert p["part_steps"] % p["stage_steps"] == 0 and nkb % p["part_steps"] == 0, where
+            assert p["chunk_steps"] == p["stage_steps"], where
+            assert 1 <= p["batch_units"] <= min(ncw, upc, 16), where
+        else:
+            cl = p["cluster"]
+            assert cl in (2, 4, 8) and p["ctas"] % cl == 0 and p["ctas"] <= SMS, where
+            # the stage divides every rank's share of the K steps
+            share = -(-nkb // cl)
+            steps = [min(nkb, (r + 1) * share) - min(nkb, r * share) for r in range(cl)]
+            assert all(s % p["stage_steps"] == 0 for s in steps), where
+            assert p["part_steps"] == 0 and p["batch_units"] == 0, where
+    assert seen == {0, 1, 2}
+
+
+def test_plan_argument_errors():
+    for args, status in [((33, 64, 8), mx.MXFP4_ERR_SHAPE), ((1, 48, 8), mx.MXFP4_ERR_SHAPE),
+                         ((0, 64, 8), mx.MXFP4_ERR_INVALID_ARG), ((1, 64, 0), mx.MXFP4_ERR_INVALID_ARG)]:
+        with pytest.raises(mx.Mxfp4Error) as e:
+            mx.linear_plan(*args, SMS, SMEM)
+        assert e.value.status == status
+    with pytest.raises(mx.Mxfp4Error) as e:
+        mx.linear_plan(4, 7168, 7168, 0, SMEM)
+    assert e.value.status == mx.MXFP4_ERR_INVALID_ARG
+
+
+def test_smaller_devices_still_plan_or_refuse():
+    """With less shared memory the planner falls back (parts, clusters) or
+    reports MXFP4_ERR_SHAPE; it never returns a plan that does not fit."""
+    for smem in (101376, 166912):
+        for t, k, n in [(4, 7168, 7168), (32, 7168, 18432), (8, 14336, 4096), (1, 1024, 1024)]:
+            try:
+                p = mx.linear_plan(t, k, n, 132, smem)
+            except mx.Mxfp4Error as e:
+                assert e.status == mx.MXFP4_ERR_SHAPE
+                continue
+            assert p["smem_bytes"] <= smem and math.gcd(p["stage_steps"], p["chunk_steps"]) == p["chunk_steps"]

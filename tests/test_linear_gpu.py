@@ -120,6 +120,28 @@ def test_linear_k_parts_many_batches_sampled():
     assert mx.last_device_status() == mx.MXFP4_OK
 
 
+@pytest.mark.parametrize("t,k,n", [(5, 6144, 12000), (3, 6176, 10000)])
+def test_linear_odd_stage_sizes_sampled(t, k, n):
+    """More than 4 row groups per SM with activations that fit: whole-stage
+    chunks of 8 / 5 steps. The second shape has K % 256 != 0 (25 steps, the
+    last one block long), fetched through the 2D tensor map. Sampled rows,
+    including the ragged tail."""
+    mx = lib()
+    plan = mx.linear_plan(t, k, n)
+    assert plan["mode"] == 0 and plan["stage_steps"] == plan["chunk_steps"] >= 5, plan
+    w, x = linear_case(100 + t, t, k, n)
+    wq, ws = mx.quantize(w)
+    y = mx.linear(x, wq, ws)
+    torch.cuda.synchronize()
+    rows = np.union1d(sample_rows(n, 384, seed=100 + t), np.arange(n - 20, n))
+    rows_t = torch.from_numpy(rows).cuda()
+    rq, rs = oracle.quantize(w[rows_t].cpu().numpy())
+    del w
+    y_ref, rss = oracle.linear(x, rq, rs)
+    assert_within(bf16_to_f64(y[:, rows_t]), y_ref, rss, f"odd stages t={t} k={k} n={n}")
+    assert mx.last_device_status() == mx.MXFP4_OK
+
+
 def test_linear_config1_full():
     """T=1, K=N=1024, seed 0: whole output against the oracle."""
     mx = lib()

@@ -23,6 +23,10 @@
 //                   Per unit, each owning warp hands its partial to a
 //                   reduction buffer; one owner sums the partials in a fixed
 //                   order and runs the problem's epilogue (deterministic).
+// K in parts (stream_kernel<P, true>, dense problem): when the activations
+// of all of K do not fit, a lone CTA walks K in parts with double-buffered
+// activation parts, and each unit of a batch stays with one consumer warp,
+// its sums in registers, across all parts.
 // Every wait is bounded (see device_common.cuh); on a timeout the kernel
 // records it in the status word and winds down.
 #pragma once
@@ -452,60 +456,38 @@ struct Placement {
     uint32_t rank, cl;
 };
 
-// One item of a CTA's work: the K steps [kb0, kb1) of one unit. Without K
-// parts an item is a whole unit over the CTA's K range.
+// K in parts: one item of a CTA's work is the K steps [kb0, kb1) of part
+// `part` of one unit.
 struct Item {
-    int u;           // unit
-    uint32_t uu;     // unit ordinal within the CTA (scale-slot sequence)
-    uint32_t j;      // unit ordinal within its batch (carry slot)
-    int part;        // K part (0 without parts)
-    bool last;       // last part of the unit
-    int q;           // K parts: activation chunk = batch * nparts + part
-    int kb0, kb1;    // K steps (256 values each)
-    int kblk0, kblk1;  // 32-blocks
+    int u;         // unit
+    uint32_t uu;   // unit ordinal within the CTA (scale-slot sequence)
+    int part;      // K part
+    int kb0, kb1;  // K steps (256 values each)
 };
 
-// The CTA's items in streaming order. K in parts (ps > 0): units are taken
-// in batches of ub; for each part, that part of every unit of the batch.
+// The CTA's items in streaming order: units in batches of ub; for each part,
+// that part of every unit of the batch.
 struct ItemSeq {
     int u0, nu;
     int ps, nparts, ub;
     int nkb, nblk;
-    int kb0, kb1, kblk0, kblk1;  // the CTA's K range without parts
-    __device__ int count() const { return ps ? nu * nparts : nu; }
-    __device__ int nchunks() const { return ps ? ((nu + ub - 1) / ub) * nparts : 0; }
+    __device__ int count() const { return nu * nparts; }
+    __device__ int nchunks() const { return ((nu + ub - 1) / ub) * nparts; }  // activation parts staged
     __device__ void part_blocks(int part, int& b0, int& b1) const {
         b0 = part * ps * 8;
         b1 = min(nblk, (part + 1) * ps * 8);
     }
     __device__ Item at(int v) const {
-        Item it;
-        if (!ps) {
-            it.u = u0 + v;
-            it.uu = static_cast<uint32_t>(v);
-            it.j = 0;
-            it.part = 0;
-            it.last = true;
-            it.q = 0;
-            it.kb0 = kb0;
-            it.kb1 = kb1;
-            it.kblk0 = kblk0;
-            it.kblk1 = kblk1;
-            return it;
-        }
         // Every batch but the last is full, so the batch is v / (ub * nparts).
         const int bi = v / (ub * nparts);
         const int r = v - bi * ub * nparts;
         const int bsize = min(ub, nu - bi * ub);
+        Item it;
         it.part = r / bsize;
-        it.j = static_cast<uint32_t>(r - it.part * bsize);
-        it.uu = static_cast<uint32_t>(bi * ub) + it.j;
+        it.uu = static_cast<uint32_t>(bi * ub + r - it.part * bsize);
         it.u = u0 + static_cast<int>(it.uu);
-        it.last = it.part == nparts - 1;
-        it.q = bi * nparts + it.part;
         it.kb0 = it.part * ps;
         it.kb1 = min(nkb, it.kb0 + ps);
-        part_blocks(it.part, it.kblk0, it.kblk1);
         return it;
     }
 };
@@ -1159,10 +1141,6 @@ __global__ void __launch_bounds__(Roles<P>::kThreads, 1)
         seq.ub = static_cast<int>(S.L.ubatch);
         seq.nkb = p.nkb;
         seq.nblk = p.nblk;
-        seq.kb0 = pl.kb0;
-        seq.kb1 = pl.kb1;
-        seq.kblk0 = pl.kblk0;
-        seq.kblk1 = pl.kblk1;
         if (warp == Roles<P>::kProducer)
             producer_parts<P>(p, S, pl, seq, &tmap, lane);
         else

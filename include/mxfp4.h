@@ -84,8 +84,10 @@ int mxfp4_quantize(const float* w, int64_t n, int64_t k, uint8_t* wq, uint8_t* w
  *   n   output features (>= 1, < 2^31)
  *   y   device bf16 [t, n], row-major, 2-byte aligned (output)
  * Accumulation is fp32 (tensor-core fp32 accumulate); the summation order
- * is the kernel's. Returns MXFP4_ERR_SHAPE when t * k is too large for the
- * on-chip activation buffer of this device.
+ * is the kernel's. Returns MXFP4_ERR_SHAPE when no shared-memory plan fits
+ * (mxfp4_linear_plan reports the plan). The binding limit is k: a row
+ * group's scale bytes for all of k (k/2 bytes) stay on chip next to the
+ * staging buffers. Every t <= 32 and n plans for k <= 262144 on GB300.
  */
 int mxfp4_linear(const void* x, int64_t t, int64_t k, const uint8_t* wq, const uint8_t* ws, int64_t n,
                  void* y, void* stream);

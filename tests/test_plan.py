@@ -114,3 +114,14 @@ def test_smaller_devices_still_plan_or_refuse():
                 assert e.status == mx.MXFP4_ERR_SHAPE
                 continue
             assert p["smem_bytes"] <= smem and math.gcd(p["stage_steps"], p["chunk_steps"]) == p["chunk_steps"]
+
+
+def test_every_token_count_plans_up_to_k_262144():
+    """The header's promise: on GB300 every t <= 32 and n plans for k up to
+    262144 (the limit is a row group's k/2 scale bytes on chip)."""
+    for t in range(1, 33):
+        for n in (1, 17, 1000, 40000, 129280):
+            for k in (262144, 262144 - 32, 131104):
+                p = mx.linear_plan(t, k, n, SMS, SMEM)
+                assert p["smem_bytes"] <= SMEM
+

@@ -142,6 +142,22 @@ def test_linear_odd_stage_sizes_sampled(t, k, n):
     assert mx.last_device_status() == mx.MXFP4_OK
 
 
+@pytest.mark.parametrize("t,k,n", [(1, 262144, 40), (32, 262144, 24)])
+def test_linear_largest_k(t, k, n):
+    """The largest k the header promises (262144): one row group's scales for
+    all of k take 128 KB of shared memory, so each CTA walks K in parts
+    (hundreds of them) with a single row group; ragged last row group."""
+    mx = lib()
+    assert mx.linear_plan(t, k, n)["mode"] == 1
+    w, x = linear_case(110 + t, t, k, n)
+    wq, ws, rq, rs = _pack_both(w)
+    y = mx.linear(x, wq, ws)
+    torch.cuda.synchronize()
+    y_ref, rss = oracle.linear(x, rq, rs)
+    assert_within(bf16_to_f64(y), y_ref, rss, f"largest k t={t} n={n}")
+    assert mx.last_device_status() == mx.MXFP4_OK
+
+
 def test_linear_config1_full():
     """T=1, K=N=1024, seed 0: whole output against the oracle."""
     mx = lib()

@@ -40,3 +40,29 @@ def linear_case(seed: int, t: int, k: int, n: int, x64: bool = False, device="cu
     w = synth.weights(seed, n, k, device=device, x64_blocks=x64)
     x = synth.tokens(seed, t, k, device=device)
     return w, x
+
+
+GUARD_BYTES = 4096
+CANARY = 0xA5
+
+
+class Guarded:
+    """A device tensor with GUARD_BYTES canary bytes on each side, so a test
+    can check that a kernel wrote nothing outside the buffer it was given
+    (the test-side stand-in for a memory checker). The tensor starts 4096
+    bytes into a fresh allocation, so it keeps the allocator's alignment."""
+
+    def __init__(self, shape, dtype, device="cuda"):
+        shape = tuple(int(s) for s in shape)
+        itemsize = torch.empty((), dtype=dtype).element_size()
+        self.nbytes = int(np.prod(shape, dtype=np.int64)) * itemsize
+        self.raw = torch.full((2 * GUARD_BYTES + self.nbytes,), CANARY, dtype=torch.uint8, device=device)
+        self.t = self.raw[GUARD_BYTES:GUARD_BYTES + self.nbytes].view(dtype).view(shape)
+
+    def check(self, what: str):
+        torch.cuda.synchronize()
+        head = self.raw[:GUARD_BYTES]
+        tail = self.raw[GUARD_BYTES + self.nbytes:]
+        bad_h = int((head != CANARY).sum())
+        bad_t = int((tail != CANARY).sum())
+        assert bad_h == 0 and bad_t == 0, f"{what}: {bad_h} guard bytes before and {bad_t} after the buffer changed"

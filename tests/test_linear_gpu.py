@@ -10,7 +10,7 @@ import torch
 import oracle
 import oracle_pins
 import synth
-from gpu_cases import assert_within, bf16_to_f64, lib, linear_case, sample_rows
+from gpu_cases import Guarded, assert_within, bf16_to_f64, lib, linear_case, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -47,8 +47,9 @@ def test_linear_small_shapes(t, k, n):
     mx = lib()
     w, x = linear_case(11 + t, t, k, n)
     wq, ws, rq, rs = _pack_both(w)
-    y = mx.linear(x, wq, ws)
-    torch.cuda.synchronize()
+    yg = Guarded((t, n), torch.bfloat16)
+    y = mx.linear(x, wq, ws, out=yg.t)
+    yg.check(f"linear t={t} k={k} n={n}")
     y_ref, rss = oracle.linear(x, rq, rs)
     assert_within(bf16_to_f64(y), y_ref, rss, f"linear t={t} k={k} n={n}")
 
@@ -59,8 +60,9 @@ def test_linear_many_tokens(t):
     k, n = 2048, 300
     w, x = linear_case(40 + t, t, k, n)
     wq, ws, rq, rs = _pack_both(w)
-    y = mx.linear(x, wq, ws)
-    torch.cuda.synchronize()
+    yg = Guarded((t, n), torch.bfloat16)
+    y = mx.linear(x, wq, ws, out=yg.t)
+    yg.check(f"linear t={t}")
     y_ref, rss = oracle.linear(x, rq, rs)
     assert_within(bf16_to_f64(y), y_ref, rss, f"linear t={t}")
 
@@ -74,8 +76,9 @@ def test_linear_cluster_split_k(t, k, n):
     mx = lib()
     w, x = linear_case(60 + t, t, k, n)
     wq, ws, rq, rs = _pack_both(w)
-    y = mx.linear(x, wq, ws)
-    torch.cuda.synchronize()
+    yg = Guarded((t, n), torch.bfloat16)
+    y = mx.linear(x, wq, ws, out=yg.t)
+    yg.check(f"cluster t={t} k={k} n={n}")
     y_ref, rss = oracle.linear(x, rq, rs)
     assert_within(bf16_to_f64(y), y_ref, rss, f"cluster t={t} k={k} n={n}")
     assert mx.last_device_status() == mx.MXFP4_OK
@@ -93,8 +96,9 @@ def test_linear_k_parts(t, k, n):
     mx = lib()
     w, x = linear_case(80 + t, t, k, n)
     wq, ws, rq, rs = _pack_both(w)
-    y = mx.linear(x, wq, ws)
-    torch.cuda.synchronize()
+    yg = Guarded((t, n), torch.bfloat16)
+    y = mx.linear(x, wq, ws, out=yg.t)
+    yg.check(f"k parts t={t} k={k} n={n}")
     y_ref, rss = oracle.linear(x, rq, rs)
     assert_within(bf16_to_f64(y), y_ref, rss, f"k parts t={t} k={k} n={n}")
     assert mx.last_device_status() == mx.MXFP4_OK

@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import synth
-from gpu_cases import assert_within, bf16_to_f64, lib
+from gpu_cases import Guarded, assert_within, bf16_to_f64, lib
 
 pytestmark = pytest.mark.gpu
 
@@ -30,13 +30,20 @@ def _experts(seed, e, hidden, inter, device="cuda"):
 
 
 def _run(x, lg, top_k, dev):
+    """One mxfp4_moe call whose outputs and workspace all sit between guard
+    bytes; checks that nothing outside them was written."""
     mx = lib()
-    t = x.shape[0]
-    ids = torch.empty((t, top_k), dtype=torch.int32, device="cuda")
-    gw = torch.empty((t, top_k), dtype=torch.float32, device="cuda")
-    y = mx.moe(x, lg, top_k, *dev, topk_ids=ids, topk_w=gw)
-    torch.cuda.synchronize()
-    return y, ids, gw
+    t, hidden = x.shape
+    e = lg.shape[1]
+    inter = dev[2].shape[2] * 2
+    ids = Guarded((t, top_k), torch.int32)
+    gw = Guarded((t, top_k), torch.float32)
+    y = Guarded((t, hidden), torch.bfloat16)
+    ws = Guarded((mx.mxfp4_moe_workspace_size(t, e, top_k, hidden, inter),), torch.uint8)
+    mx.moe(x, lg, top_k, *dev, workspace=ws.t, out=y.t, topk_ids=ids.t, topk_w=gw.t)
+    for buf, name in ((ids, "topk_ids"), (gw, "topk_w"), (y, "y"), (ws, "workspace")):
+        buf.check(f"moe t={t} e={e} top_k={top_k}: {name}")
+    return y.t, ids.t, gw.t
 
 
 @pytest.mark.parametrize("t,e,top_k,hidden,inter", [(8, 16, 4, 256, 128), (32, 64, 8, 512, 256), (1, 8, 1, 64, 32),
@@ -86,43 +93,88 @@ def test_moe_deterministic_and_status():
     assert mx.last_device_status() == mx.MXFP4_OK
 
 
-def test_moe_full_size_sampled():
-    """256 experts, W1 [4096,7168], W2 [7168,2048], T=32, top-8: routing of all
-    tokens bit-exact; sampled tokens x sampled outputs within tolerance. The
-    oracle's packings of the experts those tokens use come from the same
-    float32 weights the GPU packed."""
-    mx = lib()
+class FullSize:
+    """256 experts, W1 [4096,7168], W2 [7168,2048] packed on the device (one
+    expert generated and packed at a time), T=32 tokens, top-8."""
     t, e, top_k, hidden, inter, seed = 32, 256, 8, 7168, 2048, 4
-    w1q = torch.empty((e, 2 * inter, hidden // 2), dtype=torch.uint8, device="cuda")
-    w1s = torch.empty((e, 2 * inter, hidden // 32), dtype=torch.uint8, device="cuda")
-    w2q = torch.empty((e, hidden, inter // 2), dtype=torch.uint8, device="cuda")
-    w2s = torch.empty((e, hidden, inter // 32), dtype=torch.uint8, device="cuda")
-    for ex in range(e):  # generate and pack one expert at a time
-        a = synth.weights(seed, 2 * inter, hidden, device="cuda", row0=ex * 2 * inter)
-        q, s = mx.quantize(a)
-        w1q[ex].copy_(q.view(2 * inter, -1))
-        w1s[ex].copy_(s.view(2 * inter, -1))
-        b = synth.weights(seed, hidden, inter, tid=synth.TID_W2, device="cuda", row0=ex * hidden)
-        q, s = mx.quantize(b)
-        w2q[ex].copy_(q.view(hidden, -1))
-        w2s[ex].copy_(s.view(hidden, -1))
-    x = synth.tokens(seed, t, hidden, device="cuda")
-    lg = synth.logits(seed, t, e, device="cuda")
-    y, ids, gw = _run(x, lg, top_k, (w1q, w1s, w2q, w2s))
+
+    def __init__(self):
+        mx = lib()
+        t, e, hidden, inter, seed = self.t, self.e, self.hidden, self.inter, self.seed
+        self.w1q = torch.empty((e, 2 * inter, hidden // 2), dtype=torch.uint8, device="cuda")
+        self.w1s = torch.empty((e, 2 * inter, hidden // 32), dtype=torch.uint8, device="cuda")
+        self.w2q = torch.empty((e, hidden, inter // 2), dtype=torch.uint8, device="cuda")
+        self.w2s = torch.empty((e, hidden, inter // 32), dtype=torch.uint8, device="cuda")
+        for ex in range(e):
+            q, sc = mx.quantize(self.w1_float(ex))
+            self.w1q[ex].copy_(q.view(2 * inter, -1))
+            self.w1s[ex].copy_(sc.view(2 * inter, -1))
+            q, sc = mx.quantize(self.w2_float(ex))
+            self.w2q[ex].copy_(q.view(hidden, -1))
+            self.w2s[ex].copy_(sc.view(hidden, -1))
+        self.x = synth.tokens(seed, t, hidden, device="cuda")
+        self.lg = synth.logits(seed, t, e, device="cuda")
+        self.dev = (self.w1q, self.w1s, self.w2q, self.w2s)
+        self.W1 = {}
+
+    def w1_float(self, ex):
+        return synth.weights(self.seed, 2 * self.inter, self.hidden, device="cuda", row0=ex * 2 * self.inter)
+
+    def w2_float(self, ex):
+        return synth.weights(self.seed, self.hidden, self.inter, tid=synth.TID_W2, device="cuda",
+                             row0=ex * self.hidden)
+
+    def oracle_weights(self, experts, cols):
+        """Oracle packings, from the float32 weights, of every listed expert's
+        W1 and of the W2 rows of the sampled output columns (the oracle reads
+        no other W2 row; the rest of each array stays zero)."""
+        W2 = {}
+        for ex in experts:
+            if ex not in self.W1:
+                self.W1[ex] = oracle.quantize(self.w1_float(ex).cpu().numpy())
+            wq = np.zeros((self.hidden, self.inter // 2), np.uint8)
+            ws = np.zeros((self.hidden, self.inter // 32), np.uint8)
+            rows = self.w2_float(ex)[torch.from_numpy(cols).cuda()].cpu().numpy()
+            wq[cols], ws[cols] = oracle.quantize(rows)
+            W2[ex] = (wq, ws)
+        return {ex: self.W1[ex] for ex in experts}, W2
+
+
+@pytest.fixture(scope="module")
+def full_size():
+    return FullSize()
+
+
+def _check_full_size(fs, lg, what, ncols=512):
+    y, ids, gw = _run(fs.x, lg, fs.top_k, fs.dev)
     lgn = lg.cpu().numpy()
-    ids_ref, g_ref = oracle.route(lgn, top_k)
+    ids_ref, g_ref = oracle.route(lgn, fs.top_k)
     assert np.array_equal(ids.cpu().numpy(), ids_ref)
     assert np.allclose(gw.cpu().numpy(), g_ref, rtol=1e-6, atol=0)
-    toks = np.array([0, 13, 31])
-    cols = np.random.default_rng(0).choice(hidden, 96, replace=False)
-    need = sorted({int(v) for v in ids_ref[toks].ravel()})
-    W1, W2 = {}, {}
-    for ex in need:
-        a = synth.weights(seed, 2 * inter, hidden, device="cuda", row0=ex * 2 * inter).cpu().numpy()
-        W1[ex] = oracle.quantize(a)
-        assert np.array_equal(W1[ex][0], w1q[ex].cpu().numpy())
-        b = synth.weights(seed, hidden, inter, tid=synth.TID_W2, device="cuda", row0=ex * hidden).cpu().numpy()
-        W2[ex] = oracle.quantize(b)
-    y_ref, rss = oracle.moe(x, lgn, top_k, W1, W2, inter, tok=toks, cols=cols)
-    yg = bf16_to_f64(y)[toks][:, cols]
-    assert_within(yg, y_ref, rss, "moe full size")
+    cols = np.sort(np.random.default_rng(0).choice(fs.hidden, ncols, replace=False))
+    experts = sorted({int(v) for v in ids_ref.ravel()})
+    W1, W2 = fs.oracle_weights(experts, cols)
+    for ex in experts[:4]:  # the device packing of a few routed experts, byte for byte
+        assert np.array_equal(W1[ex][0], fs.w1q[ex].cpu().numpy())
+        assert np.array_equal(W1[ex][1], fs.w1s[ex].cpu().numpy())
+    y_ref, rss = oracle.moe(fs.x, lgn, fs.top_k, W1, W2, fs.inter, cols=cols)
+    assert_within(bf16_to_f64(y)[:, cols], y_ref, rss, what)
+    return ids_ref
+
+
+def test_moe_full_size_all_tokens_sampled_columns(full_size):
+    """The bench shape with its own seeded logits: routing of all 32 tokens
+    bit-exact, gate weights to 1e-6, and every token's output at 512 sampled
+    columns within the stated bound."""
+    _check_full_size(full_size, full_size.lg, "moe full size")
+
+
+def test_moe_full_size_hot_expert(full_size):
+    """The bench shape with 12 tokens forced onto expert 37: its gate/up
+    rows serve 12 token columns (two chunks of at most 8) and its down rows
+    12 pairs (three chunks of at most 4), so the expert is streamed once per
+    chunk at full size. Every token, 512 sampled columns."""
+    lg = full_size.lg.clone()
+    lg[:12, 37] += 8.0
+    ids_ref = _check_full_size(full_size, lg, "moe full size, hot expert")
+    assert int((ids_ref == 37).sum()) >= 12

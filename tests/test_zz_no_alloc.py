@@ -7,8 +7,8 @@ implicit synchronisation). mxfp4_moe_noalloc keeps the layer's scratch in a fixe
 array inside the library instead of a caller workspace. This file checks,
 through the C ABI, that two calls in a row (the second one reusing the
 array the first one left behind) give the same results as the workspace
-entry point, within the tolerance the other parity tests use, and that a
-problem too large for the array is refused. It is collected last so a
+entry point bit for bit and the oracle within the stated bound, and that
+a problem too large for the array is refused. It is collected last so a
 failure here does not hide any other test.
 """
 import ctypes
@@ -34,9 +34,15 @@ def _entry():
 
 
 def test_moe_noalloc_matches_workspace_entry_point_twice():
+    """Two calls in a row through the C ABI. The second one has fewer tokens
+    (fewer routed pairs) than the first, so it runs on the scratch contents
+    the first call left behind. Each call's output must be within the stated
+    bound of the oracle, and bit-identical (outputs, routing indices and gate
+    weights) to the workspace entry point on the same inputs: the kernels
+    are deterministic and only the scratch location differs."""
     mx = lib()
     noalloc = _entry()
-    t, e, top_k, hidden, inter, seed = 32, 64, 8, 1024, 512, 91
+    e, top_k, hidden, inter, seed = 64, 8, 1024, 512, 91
     w1 = synth.weights(seed, e * 2 * inter, hidden, device="cuda")
     w2 = synth.weights(seed, e * hidden, inter, tid=synth.TID_W2, device="cuda")
     w1q, w1s = mx.quantize(w1)
@@ -48,20 +54,29 @@ def test_moe_noalloc_matches_workspace_entry_point_twice():
     dev = (w1q.view(e, 2 * inter, hidden // 2), w1s.view(e, 2 * inter, hidden // 32),
            w2q.view(e, hidden, inter // 2), w2s.view(e, hidden, inter // 32))
     stream = torch.cuda.current_stream().cuda_stream
-    for call in range(2):  # the second call starts from the first call's scratch
+    for call, t in enumerate((32, 19)):
         x = synth.tokens(seed + call, t, hidden, device="cuda")
         lg = synth.logits(seed + call, t, e, device="cuda")
         ids_ws = torch.empty((t, top_k), dtype=torch.int32, device="cuda")
-        y_ws = mx.moe(x, lg, top_k, *dev, topk_ids=ids_ws)
+        gw_ws = torch.empty((t, top_k), dtype=torch.float32, device="cuda")
+        y_ws = mx.moe(x, lg, top_k, *dev, topk_ids=ids_ws, topk_w=gw_ws)
         ids_na = torch.empty((t, top_k), dtype=torch.int32, device="cuda")
+        gw_na = torch.empty((t, top_k), dtype=torch.float32, device="cuda")
         y_na = torch.empty((t, hidden), dtype=torch.bfloat16, device="cuda")
         rc = noalloc(x.data_ptr(), t, hidden, lg.data_ptr(), e, top_k, dev[0].data_ptr(), dev[1].data_ptr(),
-                     dev[2].data_ptr(), dev[3].data_ptr(), inter, y_na.data_ptr(), ids_na.data_ptr(), None, stream)
+                     dev[2].data_ptr(), dev[3].data_ptr(), inter, y_na.data_ptr(), ids_na.data_ptr(),
+                     gw_na.data_ptr(), stream)
         assert rc == mx.MXFP4_OK, mx.strerror(rc)
         torch.cuda.synchronize()
+        lgn = lg.cpu().numpy()
+        ids_ref, g_ref = oracle.route(lgn, top_k)
+        assert np.array_equal(ids_na.cpu().numpy(), ids_ref)
+        assert np.allclose(gw_na.cpu().numpy(), g_ref, rtol=1e-6, atol=0)
+        y_ref, rss = oracle.moe(x, lgn, top_k, W1, W2, inter)
+        assert_within(bf16_to_f64(y_na), y_ref, rss, f"no-alloc call {call + 1} (t={t})")
         assert torch.equal(ids_na, ids_ws)
-        _, rss = oracle.moe(x, lg.cpu().numpy(), top_k, W1, W2, inter)
-        assert_within(bf16_to_f64(y_na), bf16_to_f64(y_ws), rss, f"no-alloc call {call + 1}")
+        assert torch.equal(gw_na.view(torch.int32), gw_ws.view(torch.int32))
+        assert torch.equal(y_na.view(torch.int16), y_ws.view(torch.int16)), f"call {call + 1}: differs from mxfp4_moe"
     assert mx.last_device_status() == mx.MXFP4_OK
 
 

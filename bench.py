@@ -2,19 +2,26 @@
 """Bench: MXFP4 weight-streaming decode/verify step on GB300.
 
 One step = one weight-streaming call over one batch of decode tokens
-(default workload: T=4 verify step, K=N=7168 dense projection). Prints one
+(headline workload: T=4 verify step, K=N=7168 dense projection). Prints one
 JSON line (rank 0). Metric: effective HBM GB/s, where bytes = 0.53125*N*K
 (packed weights + scales actually read) + 2*T*K (x) + 2*T*N (y).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--sweep]
+                  [--workload NAME] [--no-workloads]
 
-Timing: the timed steps are a CUDA-graph replay of back-to-back calls that
+Timing: the timed steps are CUDA-graph replays of back-to-back calls that
 cycle through enough independent weight copies to exceed 2x L2, so every
-call streams its weights from HBM; CUDA events on the launching stream
-bracket the region (device time), and per-launch events give the kernel's
-average duration for the roofline. Clocks are sampled with nvidia-smi while
-the workload runs.
+call streams its weights from HBM. CUDA events on the launching stream
+bracket the whole region (device time); each call is one kernel launch, so
+the average launch duration behind the roofline is the region time over
+the calls (back to back, the gaps between launches included). Events
+between graph replays give the per-replay spread (p10/p50/p90 of the
+per-call time). Clocks are sampled with nvidia-smi while each workload runs.
+
+Besides the headline line's `value`, the default run times every other
+configuration of the method (the T=1 K=N=1024 linear, the LM head, the FFN
+token sweep and the grouped MoE) under a `workloads` key, each with its own
+clock summary.
 """
 from __future__ import annotations
 
@@ -185,16 +192,40 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- our arm
-def setup_dense(wl: dict, device):
+PLAN_KERNELS = {
+    0: "mxfp4::stream_kernel<DenseProblem, whole K> (mma.sync)",
+    1: "mxfp4::stream_kernel<DenseProblem, K in parts> (mma.sync)",
+    2: "mxfp4::stream_kernel<DenseProblem, cluster split of K> (mma.sync)",
+    3: "mxfp4::tc::tc_linear_kernel (tcgen05.mma kind::mxf8f6f4 block-scaled)",
+}
+
+
+def dense_kernel_name(t: int, k: int, n: int) -> str:
+    import mxfp4_weight_streaming_gb300 as mx
+    import torch
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    smem = getattr(props, "shared_memory_per_block_optin", 232448)
+    plan = mx.linear_plan(t, k, n, props.multi_processor_count, smem)
+    return PLAN_KERNELS.get(plan["mode"], f"mode {plan['mode']}") + f" [{plan['ctas']} CTAs, cluster {plan['cluster']}]"
+
+
+def setup_dense(wl: dict, device, cache=None):
     import torch
 
     import mxfp4_weight_streaming_gb300 as mx
     import synth
 
     t, k, n = wl["t"], wl["k"], wl["n"]
-    w = synth.weights(wl["seed"], n, k, device=device, x64_blocks=wl["x64"])
-    wq, ws = mx.quantize(w)
-    del w
+    key = (wl["seed"], k, n, wl["x64"])
+    if cache is not None and key in cache:
+        wq, ws = cache[key]
+    else:
+        w = synth.weights(wl["seed"], n, k, device=device, x64_blocks=wl["x64"])
+        wq, ws = mx.quantize(w)
+        del w
+        if cache is not None:
+            cache.clear()
+            cache[key] = (wq, ws)
     x = synth.tokens(wl["seed"], t, k, device=device)
     y = torch.empty((t, n), dtype=torch.bfloat16, device=device)
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
@@ -206,7 +237,63 @@ def setup_dense(wl: dict, device):
     return dict(x=x, y=y, wqs=wqs, wss=wss, copies=copies, t=t, k=k, n=n, l2=l2)
 
 
-def run_ours(args, wl_name: str, rank: int, world: int, device, with_cpu_baseline: bool):
+def percentiles(per_call_us):
+    xs = sorted(per_call_us)
+
+    def q(f):
+        return xs[min(len(xs) - 1, max(0, int(round(f * (len(xs) - 1)))))]
+
+    return {"p10": round(q(0.1), 3), "p50": round(q(0.5), 3), "p90": round(q(0.9), 3), "max": round(xs[-1], 3),
+            "replays": len(xs)}
+
+
+class GraphTimer:
+    """G back-to-back calls captured once; timed by events around the whole
+    region (the headline) and between replays (the spread)."""
+
+    def __init__(self, call, G, stream):
+        import torch
+        self.G = G
+        self.stream = stream
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                call(i)  # first calls set per-device state before capture
+        stream.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=stream):
+            for i in range(G):
+                call(i)
+
+    def soak(self, seconds):
+        import torch
+        end = time.time() + seconds
+        with torch.cuda.stream(self.stream):
+            while time.time() < end:
+                self.graph.replay()
+                self.stream.synchronize()
+        torch.cuda.synchronize()
+
+    def run(self, replays):
+        """(total ms, per-replay per-call us list)."""
+        import torch
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(replays + 1)]
+        with torch.cuda.stream(self.stream):
+            evs[0].record(self.stream)
+            for r in range(replays):
+                self.graph.replay()
+                evs[r + 1].record(self.stream)
+        evs[-1].synchronize()
+        per = [evs[r].elapsed_time(evs[r + 1]) * 1e3 / self.G for r in range(replays)]
+        return evs[0].elapsed_time(evs[-1]), per
+
+
+def gpu_index():
+    import torch
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    return torch.cuda.current_device() if vis is None else int(vis.split(",")[0])
+
+
+def run_ours(args, wl_name: str, rank: int, world: int, device, with_cpu_baseline: bool, clocks):
     import torch
 
     import mxfp4_weight_streaming_gb300 as mx
@@ -226,72 +313,34 @@ def run_ours(args, wl_name: str, rank: int, world: int, device, with_cpu_baselin
         if rc != 0:
             raise RuntimeError(mx.strerror(rc))
 
-    # Graph of G back-to-back calls (a multiple of the weight-copy count).
+    # Graph of G back-to-back calls (a multiple of the weight-copy count);
+    # the timed region is a whole number of replays.
     G = max(st["copies"], min(args.steps, 256 // st["copies"] * st["copies"] or st["copies"]))
     G = min(G, max(1, args.steps))
+    replays = max(1, args.steps // G)
+    steps = replays * G
+    timer = GraphTimer(call, G, stream)
+    timer.soak(1.0)  # keep the GPU on this workload so clock samples mean something
     with torch.cuda.stream(stream):
-        for i in range(3):
-            call(i)  # first calls set per-device state before capture
-    stream.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for i in range(G):
+        for i in range(args.warmup):
             call(i)
-    rem = args.steps % G
-    graph_rem = None
-    if rem:
-        graph_rem = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph_rem, stream=stream):
-            for i in range(rem):
-                call(i)
-    n_full = args.steps // G
-
-    clocks = ClockSampler(torch.cuda.current_device() if os.environ.get("CUDA_VISIBLE_DEVICES") is None
-                          else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[0]))
-    clocks.start()
-    # Soak: keep the GPU on this workload for ~1 s so clock samples mean something.
-    soak_end = time.time() + 1.0
-    with torch.cuda.stream(stream):
-        while time.time() < soak_end:
-            graph.replay()
-            stream.synchronize()
-        w_left = args.warmup
-        while w_left > 0:
-            if w_left >= G:
-                graph.replay()
-                w_left -= G
-            else:
-                for i in range(w_left):
-                    call(i)
-                w_left = 0
     stream.synchronize()
 
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
     wall0 = time.time()
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        for _ in range(n_full):
-            graph.replay()
-        if graph_rem is not None:
-            graph_rem.replay()
-        end.record(stream)
-    end.synchronize()
+    elapsed_ms, per_call = timer.run(replays)
     wall1 = time.time()
     torch.cuda.synchronize()
-    elapsed_ms = start.elapsed_time(end)
     if world > 1:
         elapsed_ms = reduce_max(elapsed_ms, device)
         torch.distributed.barrier()
-    clocks.stop()
 
     # End to end through the public API: pinned host x in, host y out, every step.
     x_host = st["x"].cpu().pin_memory()
     y_host = torch.empty((t, n), dtype=torch.bfloat16).pin_memory()
-    e2e_steps = max(1, min(args.steps, 2000))
+    e2e_steps = max(1, min(steps, 2000))
     with torch.cuda.stream(stream):
         for i in range(3):
             st["x"].copy_(x_host, non_blocking=True)
@@ -307,12 +356,12 @@ def run_ours(args, wl_name: str, rank: int, world: int, device, with_cpu_baselin
         e1 = time.perf_counter()
 
     bytes_call = algorithmic_bytes(t, k, n)
-    us_call = elapsed_ms * 1e3 / args.steps
-    value = job_gbps(bytes_call, args.steps, world, elapsed_ms * 1e-3)
+    us_call = elapsed_ms * 1e3 / steps
+    value = job_gbps(bytes_call, steps, world, elapsed_ms * 1e-3)
     peak, peak_src = hbm_peak()
-    # Average launch duration of the kernel over the timed region: the launches
-    # run back to back in the graph, so this includes the gaps between them.
-    avg_launch_ms = elapsed_ms / args.steps
+    # Average launch duration over the timed region: one kernel per call,
+    # launched back to back, so region time / calls (gaps included).
+    avg_launch_ms = elapsed_ms / steps
     achieved = bytes_call / (avg_launch_ms * 1e-3) / 1e9
     e2e_us = reduce_max((e1 - e0) * 1e6 / e2e_steps, device) if world > 1 else (e1 - e0) * 1e6 / e2e_steps
     res = {
@@ -320,9 +369,9 @@ def run_ours(args, wl_name: str, rank: int, world: int, device, with_cpu_baselin
         "value": round(value, 2),
         "unit": "GB/s",
         "n_gpus": world,
-        "steps": args.steps,
+        "steps": steps,
         "warmup": args.warmup,
-        "ms_per_step": elapsed_ms / args.steps,
+        "ms_per_step": elapsed_ms / steps,
         "us_per_call": round(us_call, 4),
         "pct_of_peak": round(100.0 * value / world / peak, 2),
         "higher_is_better": True,
@@ -333,16 +382,17 @@ def run_ours(args, wl_name: str, rank: int, world: int, device, with_cpu_baselin
         "config": {"workload": wl_name, "T": t, "K": k, "N": n, "bytes_per_call": bytes_call,
                    "weight_copies": st["copies"], "l2_bytes": st["l2"],
                    "l2_policy": "rotating weight copies (> 2x L2) so every call streams from HBM",
-                   "timing": f"CUDA graph replays of {G} back-to-back calls; device events around the region",
-                   "parallelism": f"replicas x{world}"},
+                   "timing": f"{replays} CUDA graph replays of {G} back-to-back calls; device events around the "
+                             f"region", "parallelism": f"replicas x{world}"},
+        "spread_us_per_call": percentiles(per_call),
         "e2e": {"value": round(job_gbps(bytes_call, 1, world, e2e_us * 1e-6), 2), "unit": "GB/s",
                 "us_per_call": round(e2e_us, 3),
                 "h2d_bytes_per_step": 2 * t * k, "d2h_bytes_per_step": 2 * t * n},
-        "gpu_launches": args.steps,
+        "gpu_launches": steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": profiled_traffic(wl_name),
                      "peak_source": f"{peak_src} (HBM copy bandwidth)",
-                     "kernel": "mxfp4::stream_kernel<DenseProblem>", "avg_launch_us": round(avg_launch_ms * 1e3, 4),
+                     "kernel": dense_kernel_name(t, k, n), "avg_launch_us": round(avg_launch_ms * 1e3, 4),
                      "algorithmic_bytes_per_launch": bytes_call},
         "clocks": clocks.summary(wall0 - 1.5, wall1 + 0.1),
     }
@@ -351,12 +401,52 @@ def run_ours(args, wl_name: str, rank: int, world: int, device, with_cpu_baselin
     return res
 
 
+def measure_dense(wl_name: str, device, cache, clocks, calls_target: int = 2000, replays: int = 12):
+    """One extra dense workload: per-call time, GB/s, fraction of peak and
+    the spread over graph replays, with its own clock samples."""
+    import torch
+
+    import mxfp4_weight_streaming_gb300 as mx
+
+    wl = WORKLOADS[wl_name]
+    st = setup_dense(wl, device, cache)
+    t, k, n = st["t"], st["k"], st["n"]
+    stream = torch.cuda.Stream(device)
+    sp = stream.cuda_stream
+    lib = mx.load()
+    xp, yp = st["x"].data_ptr(), st["y"].data_ptr()
+    wq_ptrs = [a.data_ptr() for a in st["wqs"]]
+    ws_ptrs = [a.data_ptr() for a in st["wss"]]
+
+    def call(i):
+        rc = lib.mxfp4_linear(xp, t, k, wq_ptrs[i % st["copies"]], ws_ptrs[i % st["copies"]], n, yp, sp)
+        if rc != 0:
+            raise RuntimeError(mx.strerror(rc))
+
+    G = max(st["copies"], min(256, calls_target // replays) // st["copies"] * st["copies"])
+    timer = GraphTimer(call, G, stream)
+    timer.soak(0.4)
+    wall0 = time.time()
+    ms, per_call = timer.run(replays)
+    wall1 = time.time()
+    calls = replays * G
+    nbytes = algorithmic_bytes(t, k, n)
+    us = ms * 1e3 / calls
+    peak, _ = hbm_peak()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    del st
+    return {"us_per_call": round(us, 3), "GBps": round(gbs, 1), "frac": round(gbs / peak, 4),
+            "spread_us_per_call": percentiles(per_call), "calls": calls, "bytes_per_call": nbytes,
+            "kernel": dense_kernel_name(t, k, n), "launches_per_call": 1,
+            "clocks": clocks.summary(wall0 - 0.5, wall1 + 0.1)}
+
+
 # ------------------------------------------------------------- MoE arm
 def moe_expert_bytes(hidden: int, inter: int) -> int:
     return 2 * inter * (hidden // 2 + hidden // 32) + hidden * (inter // 2 + inter // 32)
 
 
-def run_moe(steps: int, warmup: int, device):
+def run_moe(steps: int, device, clocks, replays: int = 10):
     """Grouped top-8 MoE decode step (256 experts, T=32): one mxfp4_moe call
     per step; bytes = distinct routed experts' W1+W2 (+ x, logits, y)."""
     import torch
@@ -390,38 +480,29 @@ def run_moe(steps: int, warmup: int, device):
     args = [x.data_ptr(), t, hidden, lg.data_ptr(), e, top_k, w1q.data_ptr(), w1s.data_ptr(), w2q.data_ptr(),
             w2s.data_ptr(), inter, y.data_ptr(), None, None, ws.data_ptr(), ws.numel(), stream.cuda_stream]
 
-    def call():
+    def call(i):
         rc = lib.mxfp4_moe(*args)
         if rc != 0:
             raise RuntimeError(mx.strerror(rc))
 
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            call()
-    stream.synchronize()
-    G = max(1, min(steps, 20))
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for _ in range(G):
-            call()
-    reps = max(1, steps // G)
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        for _ in range(max(1, warmup // G)):
-            graph.replay()
-        start.record(stream)
-        for _ in range(reps):
-            graph.replay()
-        end.record(stream)
-    end.synchronize()
-    ms = start.elapsed_time(end) / (reps * G)
+    G = max(1, min(steps // replays, 20))
+    timer = GraphTimer(call, G, stream)
+    timer.soak(0.5)
+    wall0 = time.time()
+    ms, per_call = timer.run(replays)
+    wall1 = time.time()
+    calls = replays * G
+    us = ms * 1e3 / calls
     nbytes = distinct * moe_expert_bytes(hidden, inter) + 2 * t * hidden + 4 * t * e + 2 * t * hidden
     peak, _ = hbm_peak()
-    gbs = nbytes / (ms * 1e-3) / 1e9
-    return {"us_per_call": round(ms * 1e3, 2), "GBps": round(gbs, 1), "pct_of_peak": round(100 * gbs / peak, 2),
-            "distinct_experts": distinct, "bytes_per_call": nbytes, "gpu_launches_per_call": 4,
-            "timing": f"CUDA graph of {G} calls (4 kernels each), device events"}
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"us_per_call": round(us, 2), "GBps": round(gbs, 1), "frac": round(gbs / peak, 4),
+            "spread_us_per_call": percentiles(per_call), "calls": calls,
+            "distinct_experts": distinct, "bytes_per_call": nbytes, "launches_per_call": 4,
+            "kernel": "mxfp4::moe_route_kernel, stream_kernel<GateUpProblem>, stream_kernel<DownProblem>, "
+                      "moe_combine_kernel",
+            "timing": f"{replays} CUDA graph replays of {G} calls (4 kernels each), device events",
+            "clocks": clocks.summary(wall0 - 0.6, wall1 + 0.1)}
 
 
 # ------------------------------------------------------- CPU oracle timing
@@ -495,7 +576,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
-    ap.add_argument("--sweep", action="store_true", help="also time every other dense workload (extra key)")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="time only the headline workload (skip the other configurations)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -521,29 +603,36 @@ def main():
     if world > 1:
         torch.distributed.barrier()
     mx.load()
+    # One clock sampler for the whole run, started before anything is timed
+    # (nvidia-smi's start-up can stall the first CUDA launches after it);
+    # each workload reads the samples of its own time window.
+    clocks = ClockSampler(gpu_index())
+    clocks.start()
+    time.sleep(2.0)
     res = run_ours(args, args.workload, rank, world, device, with_cpu_baseline=(rank == 0 and world == 1
-                                                                                 and not args.no_cpu_baseline))
-    if args.sweep and rank == 0:
-        sweep = {}
-        sub = argparse.Namespace(**vars(args))
-        sub.steps = min(args.steps, 4000)
-        sub.warmup = 50
+                                                                                 and not args.no_cpu_baseline),
+                   clocks=clocks)
+    if not args.no_workloads and rank == 0:
+        # Every other configuration, timed on rank 0 (replicas: the same on every GPU).
+        extra = {}
+        cache = {}
         for name in WORKLOADS:
             if name == args.workload:
                 continue
             try:
-                r = run_ours(sub, name, 0, 1, device, with_cpu_baseline=False)
-                sweep[name] = {"us_per_call": r["us_per_call"], "GBps": r["value"], "pct_of_peak": r["pct_of_peak"],
-                               "roofline_frac": r["roofline"]["frac"], "avg_launch_us": r["roofline"]["avg_launch_us"]}
+                extra[name] = measure_dense(name, device, cache, clocks)
             except Exception as ex:  # report, do not hide
-                sweep[name] = {"error": str(ex)[:200]}
+                extra[name] = {"error": str(ex)[:300]}
             torch.cuda.empty_cache()
-        try:
-            sweep[MOE_WORKLOAD] = run_moe(min(args.steps, 200), 5, device)
-        except Exception as ex:
-            sweep[MOE_WORKLOAD] = {"error": str(ex)[:200]}
+        cache.clear()
         torch.cuda.empty_cache()
-        res["sweep"] = sweep
+        try:
+            extra[MOE_WORKLOAD] = run_moe(200, device, clocks)
+        except Exception as ex:
+            extra[MOE_WORKLOAD] = {"error": str(ex)[:300]}
+        torch.cuda.empty_cache()
+        res["workloads"] = extra
+    clocks.stop()
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank == 0:

@@ -11,6 +11,7 @@
 #include "device_common.cuh"
 #include "linear_launch.h"
 #include "moe_launch.h"
+#include "tc_linear_launch.h"
 #include "mxfp4.h"
 
 namespace {
@@ -93,6 +94,23 @@ int encode_weight_map(CUtensorMap* map, const uint8_t* wq, int64_t rows, int64_t
     return r == CUDA_SUCCESS ? MXFP4_OK : MXFP4_ERR_CUDA;
 }
 
+// Packed weights [rows, k/2] for the block-scaled tensor-core kernel: the
+// 16U4_ALIGN16B type unpacks 16 codes per 16 bytes of shared memory (8 bytes
+// of codes, 8 of gap), the layout the MMA reads E2M1 in. The 3D view
+// (128 values, rows, k/128 atoms) with strides (k/2 B, 64 B) lets one copy
+// fetch `atoms` consecutive atoms of 128 rows: [atom][row][128 B], swizzled.
+// Needs wq 32-byte aligned and k % 128 == 0.
+int encode_tc_weight_map(CUtensorMap* map, const uint8_t* wq, int64_t rows, int64_t k, int atoms) {
+    cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(k / 128)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(k / 2), 64};
+    cuuint32_t box[3] = {128, 128, static_cast<cuuint32_t>(atoms)};
+    cuuint32_t estride[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<uint8_t*>(wq), dims, strides,
+                          box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MXFP4_OK : MXFP4_ERR_CUDA;
+}
+
 }  // namespace
 
 namespace mxfp4 {
@@ -109,8 +127,11 @@ namespace {
 struct LinearPlan {
     int dev = -1;
     const uint8_t* wq = nullptr;
+    const uint8_t* ws = nullptr;
     int64_t t = 0, k = 0, n = 0;
+    bool tc = false;  // block-scaled tensor-core kernel (else the streaming engine)
     mxfp4::LinearParams p{};
+    mxfp4::tc::TcPlan tp{};
     CUtensorMap map;
 };
 constexpr int kPlanCache = 16;
@@ -173,17 +194,26 @@ int mxfp4_linear(const void* x, int64_t t, int64_t k, const uint8_t* wq, const u
     cudaGetDevice(&dev);
     LinearPlan* plan = nullptr;
     for (LinearPlan& c : t_plans)
-        if (c.dev == dev && c.wq == wq && c.t == t && c.k == k && c.n == n) {
+        if (c.dev == dev && c.wq == wq && c.ws == ws && c.t == t && c.k == k && c.n == n) {
             plan = &c;
             break;
         }
     if (!plan) {
         LinearPlan fresh;
-        if (!linear_plan(t, k, n, d->num_sms, d->max_smem, &fresh.p.cl, &fresh.p.layout)) return MXFP4_ERR_SHAPE;
-        if (int rc = encode_weight_map(&fresh.map, wq, n, k, static_cast<int>(fresh.p.layout.steps), &fresh.p.tma3d))
-            return rc;
+        // The block-scaled tensor-core kernel when the shape and the weight
+        // alignment allow it; the streaming engine otherwise.
+        fresh.tc = aligned(wq, 32) && mxfp4::tc::plan_tc(static_cast<int>(t), k, n, d->num_sms, d->max_smem, &fresh.tp);
+        if (fresh.tc) {
+            if (int rc = encode_tc_weight_map(&fresh.map, wq, n, k, fresh.tp.atoms_per_stage)) return rc;
+        } else {
+            if (!linear_plan(t, k, n, d->num_sms, d->max_smem, &fresh.p.cl, &fresh.p.layout)) return MXFP4_ERR_SHAPE;
+            if (int rc =
+                    encode_weight_map(&fresh.map, wq, n, k, static_cast<int>(fresh.p.layout.steps), &fresh.p.tma3d))
+                return rc;
+        }
         fresh.dev = dev;
         fresh.wq = wq;
+        fresh.ws = ws;
         fresh.t = t;
         fresh.k = k;
         fresh.n = n;
@@ -191,8 +221,24 @@ int mxfp4_linear(const void* x, int64_t t, int64_t k, const uint8_t* wq, const u
         t_plan_next = (t_plan_next + 1) % kPlanCache;
         *plan = fresh;
     }
-    mxfp4::LinearParams p = plan->p;
     const CUtensorMap& map = plan->map;
+    if (plan->tc) {
+        mxfp4::tc::TcLinearParams q{};
+        q.x = static_cast<const __nv_bfloat16*>(x);
+        q.ws = ws;
+        q.y = static_cast<__nv_bfloat16*>(y);
+        q.status = d->status;
+        q.T = static_cast<int>(t);
+        q.K = static_cast<int>(k);
+        q.N = static_cast<int>(n);
+        q.nblk = static_cast<int>(k / 32);
+        q.stages = plan->tp.stages;
+        q.tiles = plan->tp.tiles;
+        q.cl = plan->tp.cl;
+        cudaError_t e = mxfp4::tc::launch_tc_linear(map, q, plan->tp, static_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
+    }
+    mxfp4::LinearParams p = plan->p;
     p.x = static_cast<const __nv_bfloat16*>(x);
     p.ws = ws;
     p.y = static_cast<__nv_bfloat16*>(y);
@@ -211,6 +257,21 @@ int mxfp4_linear(const void* x, int64_t t, int64_t k, const uint8_t* wq, const u
 int mxfp4_linear_plan(int64_t t, int64_t k, int64_t n, int num_sms, int max_smem, mxfp4_linear_plan_t* out) {
     if (!out || num_sms <= 0 || max_smem <= 0) return MXFP4_ERR_INVALID_ARG;
     if (int rc = linear_shape_status(t, k, n)) return rc;
+    mxfp4::tc::TcPlan tp{};
+    if (mxfp4::tc::plan_tc(static_cast<int>(t), k, n, num_sms, max_smem, &tp)) {
+        mxfp4_linear_plan_t r{};
+        r.mode = 3;
+        r.ctas = tp.grid;
+        r.cluster = tp.cl;
+        r.stage_steps = tp.atoms_per_stage / 2;  // 128-value atoms -> 256-value steps
+        r.chunk_steps = r.stage_steps;
+        r.ring_slots = tp.ring_slots;
+        r.part_steps = 0;
+        r.batch_units = (tp.tiles + tp.grid / tp.cl - 1) / (tp.grid / tp.cl);  // 128-row tiles per CTA (at most)
+        r.smem_bytes = tp.smem_bytes;
+        *out = r;
+        return MXFP4_OK;
+    }
     int cl = 1;
     mxfp4::SmemLayout L{};
     if (!linear_plan(t, k, n, num_sms, max_smem, &cl, &L)) return MXFP4_ERR_SHAPE;

@@ -113,6 +113,10 @@ struct StageDst {
     uint8_t* xs;
     uint8_t* fx;
     uint32_t xs_stride, fx_stride;
+    // Set to 1 when a staged block gets a factor above 1 (its largest
+    // magnitude is at least 2^15): only then can a weight scale times the
+    // factor exceed float range, and the consumers switch to the wide path.
+    volatile int* wide;
     __device__ uint8_t* col(int c, int b) const { return xs + c * xs_stride + b * 64; }
     __device__ float* factor(int c, int b) const {
         return reinterpret_cast<float*>(fx + (c >> 1) * fx_stride + b * 8 + (c & 1) * 4);
@@ -143,7 +147,8 @@ struct Pow2Scaler {
 };
 
 // Stage one block of 32 bf16 values (16 words) as f16 column data.
-__device__ __forceinline__ void stage_bf16_block(const uint32_t (&w)[16], uint8_t* dst, float* fx_out) {
+__device__ __forceinline__ void stage_bf16_block(const uint32_t (&w)[16], uint8_t* dst, float* fx_out,
+                                                 volatile int* wide) {
     // Largest magnitude: a depth-4 tree of packed 16-bit maxima.
     uint32_t m[8];
 #pragma unroll
@@ -154,6 +159,7 @@ __device__ __forceinline__ void stage_bf16_block(const uint32_t (&w)[16], uint8_
     const uint32_t amax = max(m[0] & 0xffffu, m[0] >> 16);
     int c = 0;
     if (amax != 0) c = staging_exponent(floor_log2_f32_bits(amax << 16));
+    if (c < 0) *wide = 1;
     const Pow2Scaler sc(c);
     uint32_t o[16];
     if (!sc.two) {
@@ -182,12 +188,13 @@ __device__ __forceinline__ void stage_bf16_block(const uint32_t (&w)[16], uint8_
 // Stage one block of 32 fp32 values as an exact-to-22-bits pair of f16
 // columns: hi = f16(v * 2^c), lo = f16(v * 2^c - hi). Both share the factor.
 __device__ __forceinline__ void stage_f32_block_split(const float (&v)[32], uint8_t* dst_hi, uint8_t* dst_lo,
-                                                      float* fx_hi, float* fx_lo) {
+                                                      float* fx_hi, float* fx_lo, volatile int* wide) {
     uint32_t amax = 0;
 #pragma unroll
     for (int j = 0; j < 32; ++j) amax = max(amax, __float_as_uint(v[j]) & 0x7fffffffu);
     int c = 0;
     if (amax != 0) c = staging_exponent(floor_log2_f32_bits(amax));
+    if (c < 0) *wide = 1;
     const Pow2Scaler sc(c);
     uint32_t oh[16], ol[16];
 #pragma unroll
@@ -259,7 +266,7 @@ __device__ __forceinline__ void convert_columns(int ncol, int nb, const StageDst
             w[4 * q + 2] = v.z;
             w[4 * q + 3] = v.w;
         }
-        stage_bf16_block(w, dst.col(t, b), dst.factor(t, b));
+        stage_bf16_block(w, dst.col(t, b), dst.factor(t, b), dst.wide);
         t += dt;
         b += db;
         if (t >= ncol) {
@@ -305,7 +312,10 @@ __device__ __forceinline__ bool stage_bulk(const typename P::Params& p, int chun
 // {d0, d1} (one row, two columns) is scaled and accumulated with one f32x2
 // multiply and one f32x2 FMA. acc[bx][n] = {{row g: col 2t, 2t+1}, {row g+8:
 // col 2t, 2t+1}} of n-tile n.
-template <int NT, int BOXES>
+// kWide: the weight scale and the activation factor are applied one after
+// the other in double precision, so no intermediate leaves float range
+// unless the result does (the CTA staged a block with a factor above 1).
+template <int NT, int BOXES, bool kWide = false>
 __device__ __forceinline__ void consume_step(uint32_t slot, uint32_t box_stride, uint32_t sc, int nblk, int kb,
                                              int kblk0, int kblk1, int ncols, uint32_t xs, uint32_t xs_stride,
                                              uint32_t fx, uint32_t fx_stride, uint64_t (&acc)[BOXES][NT][2],
@@ -350,8 +360,20 @@ __device__ __forceinline__ void consume_step(uint32_t slot, uint32_t box_stride,
                 for (int n = 0; n < NT; ++n) {
                     uint64_t d01, d23;
                     mma_f16_k32(d01, d23, ga, gb, xv[n]);
-                    acc[bx][n][0] = f32x2_fma(d01, f32x2_mul(W0, F[n]), acc[bx][n][0]);
-                    acc[bx][n][1] = f32x2_fma(d23, f32x2_mul(W1, F[n]), acc[bx][n][1]);
+                    if constexpr (kWide) {
+                        const float2 f = f32x2_unpack(F[n]);
+                        const float2 a = f32x2_unpack(d01), c = f32x2_unpack(d23);
+                        float2 s0 = f32x2_unpack(acc[bx][n][0]), s1 = f32x2_unpack(acc[bx][n][1]);
+                        s0.x += static_cast<float>(static_cast<double>(a.x) * fw0 * f.x);
+                        s0.y += static_cast<float>(static_cast<double>(a.y) * fw0 * f.y);
+                        s1.x += static_cast<float>(static_cast<double>(c.x) * fw1 * f.x);
+                        s1.y += static_cast<float>(static_cast<double>(c.y) * fw1 * f.y);
+                        acc[bx][n][0] = f32x2_pack(s0.x, s0.y);
+                        acc[bx][n][1] = f32x2_pack(s1.x, s1.y);
+                    } else {
+                        acc[bx][n][0] = f32x2_fma(d01, f32x2_mul(W0, F[n]), acc[bx][n][0]);
+                        acc[bx][n][1] = f32x2_fma(d23, f32x2_mul(W1, F[n]), acc[bx][n][1]);
+                    }
                 }
             }
         }
@@ -500,6 +522,7 @@ struct Smem {
     SmemLayout L;
     Bars bars;
     WaitCtx wait;
+    volatile int* wide;  // see StageDst::wide
 };
 
 template <class P>
@@ -756,7 +779,7 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
             __syncwarp();
             if (lane == 0) mbar_arrive(bars.xbar(0));
             if (!warp_wait(bars.xbar(0), xphase & 1, S.wait)) return;
-            const StageDst dst{xs, reinterpret_cast<uint8_t*>(fx), L.xs_stride, L.fx_stride};
+            const StageDst dst{xs, reinterpret_cast<uint8_t*>(fx), L.xs_stride, L.fx_stride, S.wide};
             if constexpr (P::kBulkStage) {
                 if (!stage_bulk<P>(p, chunk, pl.kblk0, pl.kblk1, dst, xs_s, bars.xbar(2), xphase & 1, S.wait,
                                    warp * 32 + lane, Roles<P>::kConsumerThreads))
@@ -798,8 +821,12 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
                 if (!warp_wait(bars.full(slot), phase, S.wait)) return;
                 uint32_t step_smem = ring + slot * stage_bytes + within * G * kBoxBytes;
                 int kb = pl.kb0 + static_cast<int>((c - cb) * G);
+                const bool wide = *S.wide != 0;  // stable once this chunk's activations are staged
                 for (uint32_t st = 0; st < G; ++st, ++kb, step_smem += kBoxBytes) {
-                    if (fast_steps && kb * 8 + 8 <= pl.kblk1)
+                    if (wide)
+                        consume_step<NT, BOXES, true>(step_smem, box_stride, sc, p.nblk, kb, pl.kblk0, pl.kblk1,
+                                                      ncols, xs_s, L.xs_stride, fx_s, L.fx_stride, acc, lane);
+                    else if (fast_steps && kb * 8 + 8 <= pl.kblk1)
                         consume_step_full<NT, BOXES>(step_smem, box_stride, sc, p.nblk, kb, pl.kblk0, ncols, xs_s,
                                                      L.xs_stride, fx_s, L.fx_stride, acc, lane);
                     else
@@ -973,7 +1000,7 @@ __device__ void consumer_parts(const typename P::Params& p, const Smem& S, const
             const uint32_t b = static_cast<uint32_t>(q) & 1u;
             const uint32_t par = (static_cast<uint32_t>(q) >> 1) & 1u;
             if (!warp_wait(bars.xbar(b), par, S.wait)) return;
-            const StageDst dst{xs + b * L.xs_buf, fx + b * L.fx_buf, L.xs_stride, L.fx_stride};
+            const StageDst dst{xs + b * L.xs_buf, fx + b * L.fx_buf, L.xs_stride, L.fx_stride, S.wide};
             convert_columns<8 * NT>(P::stage_cols(p, 0), kblk1 - kblk0, dst, xs_s + b * L.xs_buf, tid,
                                     Roles<P>::kConsumerThreads);
             __syncwarp();
@@ -1001,8 +1028,12 @@ __device__ void consumer_parts(const typename P::Params& p, const Smem& S, const
                 if (!__all_sync(0xffffffffu, wait_shared_value(bars.ring_tag(slot), stage, S.wait))) return;
                 if (!warp_wait(bars.full(slot), phase, S.wait)) return;
                 uint32_t step_smem = ring + slot * stage_bytes;
+                const bool wide = *S.wide != 0;  // stable once this part's activations are staged
                 for (uint32_t st = 0; st < spb; ++st, ++kb, step_smem += kBoxBytes) {
-                    if (fast_steps && kb * 8 + 8 <= kblk1)
+                    if (wide)
+                        consume_step<NT, BOXES, true>(step_smem, box_stride, sc, p.nblk, kb, kblk0, kblk1, ncols,
+                                                      xcur, L.xs_stride, fcur, L.fx_stride, acc, lane);
+                    else if (fast_steps && kb * 8 + 8 <= kblk1)
                         consume_step_full<NT, BOXES>(step_smem, box_stride, sc, p.nblk, kb, kblk0, ncols, xcur,
                                                      L.xs_stride, fcur, L.fx_stride, acc, lane);
                     else
@@ -1066,6 +1097,7 @@ __global__ void __launch_bounds__(Roles<P>::kThreads, 1)
     S.L = p.layout;
     S.bars = Bars{S.base + S.L.bars, S.L.nslot, S.L.nss, S.L.nrb, S.base + S.L.tags};
     S.wait = WaitCtx{p.status, reinterpret_cast<volatile int*>(S.gbase + (S.bars.abort_flag() - S.base))};
+    S.wide = reinterpret_cast<volatile int*>(S.gbase + (S.bars.abort_flag() + 4 - S.base));
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -1119,7 +1151,10 @@ __global__ void __launch_bounds__(Roles<P>::kThreads, 1)
             if (lane < 2) mbar_init(bars.xbar(lane), P::NCW);  // staging
             if (lane == 2) mbar_init(bars.xbar(2), 1);
         }
-        if (lane == 4) *S.wait.abort = 0;
+        if (lane == 4) {
+            *S.wait.abort = 0;
+            *S.wide = 0;
+        }
         fence_barrier_init();  // visible to the bulk-copy (async) proxy and to cluster peers
     }
     if (pl.cl > 1)

@@ -383,7 +383,8 @@ struct DownProblem {
                 v[4 * k + 2] = f.z;
                 v[4 * k + 3] = f.w;
             }
-            stage_f32_block_split(v, dst.col(t, b), dst.col(cnt + t, b), dst.factor(t, b), dst.factor(cnt + t, b));
+            stage_f32_block_split(v, dst.col(t, b), dst.col(cnt + t, b), dst.factor(t, b), dst.factor(cnt + t, b),
+                                  dst.wide);
         }
         for (int it = tid; it < nb * (8 - 2 * cnt); it += nthreads) {
             const int b = it / (8 - 2 * cnt);

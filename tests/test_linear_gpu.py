@@ -2,6 +2,11 @@
 
 Packing is compared byte for byte; outputs elementwise under the stated
 bound |y - y_ref| <= 4e-3*|y_ref| + 1e-3*sqrt(sum_k (x_k*w_k)^2).
+
+mxfp4_linear has two kernels: the block-scaled tensor-core kernel for
+t >= 5 and k % 512 == 0 (plan mode 3) and the streaming engine otherwise
+(modes 0-2). Shapes below cover both; k % 512 != 0 twins keep the engine's
+whole-K, K-in-parts and cluster modes under test at t >= 5.
 """
 import numpy as np
 import pytest
@@ -54,10 +59,10 @@ def test_linear_small_shapes(t, k, n):
     assert_within(bf16_to_f64(y), y_ref, rss, f"linear t={t} k={k} n={n}")
 
 
-@pytest.mark.parametrize("t", [9, 16, 23, 32])
-def test_linear_many_tokens(t):
+@pytest.mark.parametrize("t,k", [(9, 2048), (16, 2048), (23, 2048), (32, 2048), (9, 2080), (32, 2080)])
+def test_linear_many_tokens(t, k):
     mx = lib()
-    k, n = 2048, 300
+    n = 300
     w, x = linear_case(40 + t, t, k, n)
     wq, ws, rq, rs = _pack_both(w)
     yg = Guarded((t, n), torch.bfloat16)
@@ -68,11 +73,15 @@ def test_linear_many_tokens(t):
 
 
 @pytest.mark.parametrize("t,k,n", [(16, 7168, 130), (32, 7168, 70), (24, 14336, 40), (8, 16384, 33),
-                                   (12, 30720, 17)])
+                                   (12, 30720, 17), (16, 7200, 130), (8, 16416, 33)])
 def test_linear_cluster_split_k(t, k, n):
-    """Token counts whose staged activations exceed one SM, with one row group
-    per CTA: K is split over a thread-block cluster and the partial sums meet
-    through DSMEM."""
+    """Few output rows for many tokens and a long K: K is split over the two
+    CTAs of a cluster and the partial sums meet through distributed shared
+    memory (tensor-core kernel for k % 512 == 0; the engine's cluster mode
+    for the last two shapes)."""
+    mx = lib()
+    plan = mx.linear_plan(t, k, n)
+    assert plan["cluster"] == 2 or plan["mode"] == 1, plan
     mx = lib()
     w, x = linear_case(60 + t, t, k, n)
     wq, ws, rq, rs = _pack_both(w)
@@ -84,16 +93,19 @@ def test_linear_cluster_split_k(t, k, n):
     assert mx.last_device_status() == mx.MXFP4_OK
 
 
-@pytest.mark.parametrize("t,k,n", [(16, 7168, 4900), (32, 7200, 4900), (12, 7168, 4864), (17, 4096, 5000),
-                                   (24, 14336, 4900)])
+@pytest.mark.parametrize("t,k,n", [(16, 7200, 4900), (32, 7200, 4900), (12, 7200, 4864), (17, 4128, 5000),
+                                   (24, 14368, 4900), (16, 7168, 4900), (17, 4096, 5000)])
 def test_linear_k_parts(t, k, n):
-    """Token counts whose activations over all of K leave no useful ring in
-    one SM, with at least 2 row groups per CTA: each CTA walks K in parts
-    (double-buffered activation parts; each row group's sums stay with one
-    warp across the parts). Covers a ragged row group, K % 256 != 0 (29
-    one-step parts, the last one block long), partial token tiles (12 of 16,
-    17 of 32) and CTAs with fewer row groups than warps."""
+    """Streaming engine (k % 512 != 0), token counts whose activations over
+    all of K leave no useful ring in one SM, with at least 2 row groups per
+    CTA: each CTA walks K in parts (double-buffered activation parts; each
+    row group's sums stay with one warp across the parts). Covers a ragged
+    row group, K % 256 != 0 (29 one-step parts, the last one block long),
+    partial token tiles (12 of 16, 17 of 32) and CTAs with fewer row groups
+    than warps. The last two shapes are the same sizes on the tensor-core
+    kernel (2-CTA clusters over 39-40 tiles of 128 rows, ragged last tile)."""
     mx = lib()
+    assert mx.linear_plan(t, k, n)["mode"] == (1 if k % 512 else 3)
     w, x = linear_case(80 + t, t, k, n)
     wq, ws, rq, rs = _pack_both(w)
     yg = Guarded((t, n), torch.bfloat16)
@@ -104,13 +116,16 @@ def test_linear_k_parts(t, k, n):
     assert mx.last_device_status() == mx.MXFP4_OK
 
 
-def test_linear_k_parts_many_batches_sampled():
-    """T=32, K=4096, N=40008: 16-17 row groups per CTA in batches of 8 (one
-    per consumer warp), so every CTA re-stages the activation parts per
-    batch and a CTA with 17 ends on a one-unit batch; sampled rows
-    (including the ragged last group of 8) against the oracle."""
+@pytest.mark.parametrize("k", [4128, 4096])
+def test_linear_k_parts_many_batches_sampled(k):
+    """T=32, N=40008. K=4128 (streaming engine): 16-17 row groups per CTA in
+    batches of 8 (one per consumer warp), so every CTA re-stages the
+    activation parts per batch and a CTA with 17 ends on a one-unit batch.
+    K=4096 (tensor-core kernel): 313 tiles of 128 rows, 2-3 per CTA, the
+    last one 72 rows. Sampled rows (including the ragged tail) against the
+    oracle."""
     mx = lib()
-    t, k, n = 32, 4096, 40008
+    t, n = 32, 40008
     w, x = linear_case(90, t, k, n)
     wq, ws = mx.quantize(w)
     y = mx.linear(x, wq, ws)
@@ -124,12 +139,12 @@ def test_linear_k_parts_many_batches_sampled():
     assert mx.last_device_status() == mx.MXFP4_OK
 
 
-@pytest.mark.parametrize("t,k,n", [(5, 6144, 12000), (3, 6176, 10000)])
+@pytest.mark.parametrize("t,k,n", [(5, 6112, 12000), (3, 6176, 10000)])
 def test_linear_odd_stage_sizes_sampled(t, k, n):
-    """More than 4 row groups per SM with activations that fit: whole-stage
-    chunks of 8 / 5 steps. The second shape has K % 256 != 0 (25 steps, the
-    last one block long), fetched through the 2D tensor map. Sampled rows,
-    including the ragged tail."""
+    """Streaming engine, more than 4 row groups per SM with activations that
+    fit: whole-stage chunks of 8 / 5 steps. Both shapes have K % 256 != 0
+    (24 and 25 steps, the last one a partial step), fetched through the 2D
+    tensor map. Sampled rows, including the ragged tail."""
     mx = lib()
     plan = mx.linear_plan(t, k, n)
     assert plan["mode"] == 0 and plan["stage_steps"] == plan["chunk_steps"] >= 5, plan
@@ -146,13 +161,15 @@ def test_linear_odd_stage_sizes_sampled(t, k, n):
     assert mx.last_device_status() == mx.MXFP4_OK
 
 
-@pytest.mark.parametrize("t,k,n", [(1, 262144, 40), (32, 262144, 24)])
+@pytest.mark.parametrize("t,k,n", [(1, 262144, 40), (32, 262144, 24), (1, 262112, 40), (32, 262112, 24)])
 def test_linear_largest_k(t, k, n):
-    """The largest k the header promises (262144): one row group's scales for
-    all of k take 128 KB of shared memory, so each CTA walks K in parts
-    (hundreds of them) with a single row group; ragged last row group."""
+    """The largest k the header promises (262144). Tensor-core kernel: one
+    tile shared by a 2-CTA cluster, 256 stages per CTA. Streaming engine
+    (k = 262112): one row group's scales for all of k take 128 KB of shared
+    memory, so each CTA walks K in parts (hundreds of them) with a single
+    row group; ragged last row group."""
     mx = lib()
-    assert mx.linear_plan(t, k, n)["mode"] == 1
+    assert mx.linear_plan(t, k, n)["mode"] == (3 if k % 512 == 0 and t >= 5 else 1)
     w, x = linear_case(110 + t, t, k, n)
     wq, ws, rq, rs = _pack_both(w)
     y = mx.linear(x, wq, ws)
@@ -173,23 +190,27 @@ def test_linear_config1_full():
     assert_within(bf16_to_f64(y), y_ref, rss, "config 1")
 
 
-def test_linear_verify_t4_full():
-    """T=4, K=N=7168 (one target + three drafts): whole output."""
+@pytest.mark.parametrize("t", [4, 8])
+def test_linear_verify_full(t):
+    """K=N=7168, whole output: T=4 (one target + three drafts; streaming
+    engine) and T=8 (tensor-core kernel, 2-CTA clusters)."""
     mx = lib()
-    w, x = linear_case(1, 4, 7168, 7168)
+    w, x = linear_case(1, t, 7168, 7168)
     wq, ws, rq, rs = _pack_both(w)
     assert np.array_equal(wq.cpu().numpy(), rq) and np.array_equal(ws.cpu().numpy(), rs)
     y = mx.linear(x, wq, ws)
     torch.cuda.synchronize()
     y_ref, rss = oracle.linear(x, rq, rs)
-    assert_within(bf16_to_f64(y), y_ref, rss, "verify t=4")
+    assert_within(bf16_to_f64(y), y_ref, rss, f"verify t={t}")
 
 
-def test_linear_lmhead_full_size_sampled():
-    """LM head T=4, K=7168, N=129280 with 1% of blocks x64: packing of sampled
-    rows bit-exact, sampled output rows within tolerance."""
+@pytest.mark.parametrize("t", [4, 6])
+def test_linear_lmhead_full_size_sampled(t):
+    """LM head K=7168, N=129280 with 1% of blocks x64 (T=4 as configured;
+    T=6 runs the tensor-core kernel, 6-7 tiles per CTA in one batch):
+    packing of sampled rows bit-exact, sampled output rows within tolerance."""
     mx = lib()
-    t, k, n = 4, 7168, 129280
+    k, n = 7168, 129280
     w, x = linear_case(2, t, k, n, x64=True)
     wq, ws = mx.quantize(w)
     y = mx.linear(x, wq, ws)
@@ -221,12 +242,14 @@ def test_linear_ffn_sweep_sampled(t):
     assert_within(bf16_to_f64(y[:, rows_t]), y_ref, rss, f"ffn t={t}")
 
 
-def test_linear_extreme_scales():
+@pytest.mark.parametrize("t,k", [(5, 512), (3, 512), (3, 544)])
+def test_linear_extreme_scales(t, k):
     """Blocks with scale bytes 0, 1, 2, 250, 252 and 254 next to ordinary ones;
-    activations chosen so every exact output stays inside bf16 range."""
+    activations chosen so every exact output stays inside bf16 range (both
+    kernels: t = 5, k = 512 tensor core; t = 3 streaming engine)."""
     mx = lib()
     rng = np.random.default_rng(5)
-    t, k, n = 3, 512, 64
+    n = 64
     rq = rng.integers(0, 256, (n, k // 2), dtype=np.uint8)
     rs = rng.integers(120, 135, (n, k // 32), dtype=np.uint8)
     xs = rng.normal(0, 1, (t, k)).astype(np.float32)
@@ -245,11 +268,13 @@ def test_linear_extreme_scales():
     assert_within(bf16_to_f64(y), y_ref, rss, "extreme scales")
 
 
-def test_linear_activation_extremes():
-    """bf16 activations spanning subnormal to 2^120, and all-zero blocks."""
+@pytest.mark.parametrize("t,k", [(4, 1024), (6, 1024), (6, 1056)])
+def test_linear_activation_extremes(t, k):
+    """bf16 activations spanning subnormal to 2^120, and all-zero blocks
+    (both kernels: t = 6, k = 1024 tensor core)."""
     mx = lib()
     rng = np.random.default_rng(6)
-    t, k, n = 4, 1024, 96
+    n = 96
     xs = rng.normal(0, 1, (t, k)) * 2.0 ** rng.integers(-130, 100, (t, k // 32)).repeat(32, axis=1)
     xs[1, 64:96] = 0.0
     xs = np.clip(xs, -1e35, 1e35).astype(np.float32)
@@ -262,9 +287,10 @@ def test_linear_activation_extremes():
     assert_within(bf16_to_f64(y), y_ref, rss, "activation extremes")
 
 
-def test_linear_deterministic():
+@pytest.mark.parametrize("t", [4, 8])
+def test_linear_deterministic(t):
     mx = lib()
-    w, x = linear_case(8, 4, 7168, 2048)
+    w, x = linear_case(8, t, 7168, 2048)
     wq, ws = mx.quantize(w)
     y1 = mx.linear(x, wq, ws)
     y2 = mx.linear(x, wq, ws)
@@ -278,3 +304,44 @@ def test_linear_no_device_timeout():
     wq, ws = mx.quantize(w)
     mx.linear(x, wq, ws)
     assert mx.last_device_status() == mx.MXFP4_OK
+
+
+@pytest.mark.parametrize("t,k", [(6, 512), (2, 512), (2, 544)])
+def test_linear_scale_times_activation_factor_no_overflow(t, k):
+    """Blocks with weight scale 2^127 (s = 254) whose nonzero codes meet
+    small activations, while a larger activation of the same 32-block meets
+    a zero code. The exact result is finite, but the weight scale times the
+    activation block's own power-of-two factor reaches 2^128: no kernel may
+    form that product on its way to the result. The large activation is 2^8
+    (tensor-core kernel, t = 6: its activation scale is 2^1) and 2^16
+    (streaming engine, t = 2: its staging factor is 2^2); the small ones
+    are +-2^-5 times a 4-bit significand, so every piece of them stays
+    exact, and the weight codes of the block are +-0.5, which keeps every
+    exact output below 2^127."""
+    mx = lib()
+    rng = np.random.default_rng(12)
+    n = 48
+    big = 2.0 ** 8 if mx.linear_plan(t, k, n)["mode"] == 3 else 2.0 ** 16
+    rq = rng.integers(0, 256, (n, k // 2), dtype=np.uint8)
+    rs = rng.integers(120, 126, (n, k // 32), dtype=np.uint8)
+    xs = rng.normal(0, 1, (t, k)).astype(np.float32)
+    b0 = 3  # the extreme block
+    xs[:, b0 * 32:(b0 + 1) * 32] = (2.0 ** -5) * (1 + rng.integers(0, 8, (t, 32)) / 8.0) * \
+        rng.choice([-1.0, 1.0], (t, 32))
+    xs[:, b0 * 32 + 5] = big
+    codes = np.zeros((n, 32), np.uint8)
+    codes[:, :] = rng.choice([1, 9], (n, 32))  # +-0.5
+    codes[:, 5] = 0                                   # the large activation meets a zero weight
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    rq[:, b0 * 16:(b0 + 1) * 16] = packed
+    rs[:, b0] = 254
+    x = torch.from_numpy(xs).to(torch.bfloat16)
+    blk = slice(b0 * 32, (b0 + 1) * 32)
+    assert np.array_equal(x.float().numpy()[:, blk], xs[:, blk])  # the constructed block is exact in bf16
+    y = mx.linear(x.cuda(), torch.from_numpy(rq).cuda(), torch.from_numpy(rs).cuda())
+    torch.cuda.synchronize()
+    y_ref, rss = oracle.linear(x, rq, rs)
+    assert np.all(np.isfinite(y_ref)) and np.all(np.abs(y_ref) < 2.0 ** 127)
+    yg = bf16_to_f64(y)
+    assert np.all(np.isfinite(yg)), "overflow"
+    assert_within(yg, y_ref, rss, f"scale x factor, k={k}")

@@ -1,6 +1,8 @@
-"""The launch plans of mxfp4_linear, checked on the host (no GPU): the choice
-between whole K per CTA, K walked in parts and a cluster split of K, and the
-invariants every plan must keep for the kernel's indexing to hold."""
+"""The launch plans of mxfp4_linear, checked on the host (no GPU): which
+kernel a shape gets (the block-scaled tensor-core kernel when t >= 5 and
+k % 512 == 0, else the streaming engine with whole K per CTA, K walked in
+parts or a cluster split of K), and the invariants every plan must keep for
+the kernel's indexing to hold."""
 import math
 
 import pytest
@@ -21,17 +23,35 @@ def consumer_warps(t):
     return 14 if t <= 8 else (12 if t <= 16 else 8)
 
 
+@pytest.mark.parametrize("t,k,n,cluster,ctas", [
+    (8, 7168, 7168, 2, 112),        # 56 tiles of 128 rows, K split over 2-CTA clusters
+    (5, 1024, 1024, 2, 16),
+    (8, 7168, 18432, 1, 144),       # FFN up: one tile per CTA
+    (32, 7168, 18432, 1, 144),
+    (6, 7168, 129280, 1, 152),      # LM-head width: 1010 tiles over every SM
+    (16, 7168, 4900, 2, 78),
+])
+def test_tensor_core_plans(t, k, n, cluster, ctas):
+    p = mx.linear_plan(t, k, n, SMS, SMEM)
+    assert p["mode"] == 3, p
+    assert (p["cluster"], p["ctas"]) == (cluster, ctas), p
+    tiles = -(-n // 128)
+    per_cta = -(-tiles // (ctas // cluster))
+    assert p["batch_units"] == per_cta and p["part_steps"] == 0, p
+
+
 @pytest.mark.parametrize("t,k,n,mode,stage,chunk,part,batch", [
-    (4, 7168, 7168, 0, 4, 4, 0, 0),      # verify: 3 row groups per CTA, 4-step stages and chunks
+    (4, 7168, 7168, 0, 4, 4, 0, 0),      # t <= 4: streaming engine; verify: 3 row groups per CTA, 4-step stages
     (1, 1024, 1024, 0, 4, 1, 0, 0),      # one row group of 4 steps per CTA: 1-step chunks
     (1, 7168, 18432, 0, 7, 7, 0, 0),     # FFN up, whole-stage chunks
-    (8, 7168, 18432, 0, 7, 7, 0, 0),
     (4, 7168, 129280, 0, 7, 7, 0, 0),    # LM head
-    (16, 7168, 18432, 1, 4, 4, 4, 8),    # activations of all of K fill shared memory: K in parts
-    (32, 7168, 18432, 1, 2, 2, 2, 8),
+    (4, 7200, 7168, 0, 1, 1, 0, 0),      # k % 512 != 0: 29 K steps (prime): 1-step stages
+    (1, 1056, 1024, 0, 1, 1, 0, 0),      # 5 K steps, the last one block long
+    (8, 6176, 18432, 0, 5, 5, 0, 0),     # 25 K steps: whole 5-step stage chunks
+    (32, 7200, 18432, 1, 1, 1, 1, 8),    # activations of all of K fill shared memory: K in parts
     (32, 7200, 4900, 1, 1, 1, 1, 3),     # 29 K steps (prime): one-step parts
 ])
-def test_plan_choices(t, k, n, mode, stage, chunk, part, batch):
+def test_streaming_engine_plans(t, k, n, mode, stage, chunk, part, batch):
     p = mx.linear_plan(t, k, n, SMS, SMEM)
     assert (p["mode"], p["stage_steps"], p["chunk_steps"], p["part_steps"], p["batch_units"]) == \
         (mode, stage, chunk, part, batch), p
@@ -39,15 +59,15 @@ def test_plan_choices(t, k, n, mode, stage, chunk, part, batch):
 
 
 def test_cluster_only_for_single_row_group_ctas():
-    p = mx.linear_plan(16, 7168, 130, SMS, SMEM)
+    p = mx.linear_plan(16, 7200, 130, SMS, SMEM)
     assert p["mode"] == 2 and p["cluster"] == 2 and p["ctas"] == 2 * 9
-    p = mx.linear_plan(16, 7168, 4900, SMS, SMEM)  # 2-3 row groups per CTA
+    p = mx.linear_plan(16, 7200, 4900, SMS, SMEM)  # 2-3 row groups per CTA
     assert p["mode"] == 1
 
 
 def grid():
     for t in (1, 2, 3, 4, 5, 8, 9, 12, 16, 17, 23, 24, 32):
-        for k in (32, 96, 1024, 1056, 2048, 4096, 7168, 7200, 14336, 16384):
+        for k in (32, 96, 1024, 1056, 2048, 4096, 7168, 7200, 14336, 16384, 30720, 6176):
             for n in (1, 17, 130, 1024, 4900, 18432, 129280):
                 yield t, k, n
 
@@ -61,12 +81,24 @@ def test_plan_invariants_over_shapes():
             assert e.status == mx.MXFP4_ERR_SHAPE
             continue
         seen.add(p["mode"])
+        where = f"t={t} k={k} n={n}: {p}"
+        assert p["smem_bytes"] <= SMEM, where
+        if p["mode"] == 3:
+            # tensor-core kernel: t >= 5, k % 512, 128-row tiles, one tile
+            # per 2-CTA cluster or a tile range per CTA, 2- or 4-atom stages
+            tiles = -(-n // 128)
+            assert k % 512 == 0 and t >= 5, where
+            assert p["stage_steps"] in (1, 2) and p["ring_slots"] >= 2, where
+            if p["cluster"] == 2:
+                assert p["ctas"] == 2 * tiles and 2 * tiles <= SMS and p["batch_units"] == 1, where
+            else:
+                assert p["cluster"] == 1 and p["ctas"] == min(SMS, tiles), where
+            continue
+        assert k % 512 != 0 or t <= 4, where
         nkb = -(-k // 256)
         n_rg = -(-n // 16)
         upc = -(-n_rg // min(SMS, n_rg))
         ncw = consumer_warps(t)
-        where = f"t={t} k={k} n={n}: {p}"
-        assert p["smem_bytes"] <= SMEM, where
         assert p["stage_steps"] >= 1 and p["stage_steps"] % p["chunk_steps"] == 0, where
         assert p["ring_slots"] >= 2, where
         if p["mode"] == 0:
@@ -89,7 +121,7 @@ def test_plan_invariants_over_shapes():
             steps = [min(nkb, (r + 1) * share) - min(nkb, r * share) for r in range(cl)]
             assert all(s % p["stage_steps"] == 0 for s in steps), where
             assert p["part_steps"] == 0 and p["batch_units"] == 0, where
-    assert seen == {0, 1, 2}
+    assert seen == {0, 1, 2, 3}
 
 
 def test_plan_argument_errors():

@@ -39,6 +39,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+/* The library is built with hidden visibility; only these declarations are
+ * exported, so two builds loaded into one process never share a symbol. */
+#if defined(__GNUC__)
+#pragma GCC visibility push(default)
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -198,6 +204,10 @@ int mxfp4_last_device_status(void* stream);
 
 #ifdef __cplusplus
 }
+#endif
+
+#if defined(__GNUC__)
+#pragma GCC visibility pop
 #endif
 
 #endif /* MXFP4_H */

@@ -15,6 +15,7 @@ BUILD_DIR = os.path.join(HERE, "_build")
 SOURCES = ["quantize.cu", "linear.cu", "moe.cu", "capi.cu", "moe_noalloc.cu", "tc_linear.cu"]
 NVCC = os.environ.get("NVCC", os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc"))
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-gencode", "arch=compute_103a,code=sm_103a", "-Xcompiler", "-fPIC",
+         "-Xcompiler", "-fvisibility=hidden",
          "-I", INCLUDE, "-I", CSRC]
 
 
@@ -32,15 +33,26 @@ def _digest() -> str:
 
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile every translation unit and link libmxfp4.so; returns its path."""
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    stamp = os.path.join(BUILD_DIR, "stamp")
-    digest = _digest()
-    if not force and os.path.exists(LIB) and os.path.exists(stamp) and open(stamp).read() == digest:
-        return LIB
+    return _build(LIB, BUILD_DIR, [], force, verbose)
+
+
+def build_test_variant(name: str, defines: list[str]) -> str:
+    """A test-only copy of the library compiled with extra -D definitions,
+    under _build/<name>/ (never the product libmxfp4.so); returns its path."""
+    out_dir = os.path.join(BUILD_DIR, name)
+    return _build(os.path.join(out_dir, f"libmxfp4_{name}.so"), out_dir, [f"-D{d}" for d in defines], False, False)
+
+
+def _build(lib: str, build_dir: str, extra: list[str], force: bool, verbose: bool) -> str:
+    os.makedirs(build_dir, exist_ok=True)
+    stamp = os.path.join(build_dir, "stamp")
+    digest = _digest() + " ".join(extra)
+    if not force and os.path.exists(lib) and os.path.exists(stamp) and open(stamp).read() == digest:
+        return lib
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
-        cmd = [NVCC, *FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        obj = os.path.join(build_dir, src.replace(".cu", ".o"))
+        cmd = [NVCC, *FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.append("-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -52,15 +64,15 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     r = subprocess.run([NVCC, "-shared", "-gencode", "arch=compute_103a,code=sm_103a", *objs, "-o", tmp],
                        capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp, "w") as f:
         f.write(digest)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

@@ -9,8 +9,26 @@
 
 namespace mxfp4 {
 
-// Every spin-wait gives up after this many nanoseconds of %globaltimer.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
+// Every spin-wait gives up after this many nanoseconds of %globaltimer. A
+// test-only build shortens it (see MXFP4_TEST_WITHHOLD_STAGE).
+#ifndef MXFP4_WAIT_LIMIT_NS
+#define MXFP4_WAIT_LIMIT_NS 2000000000ull
+#endif
+constexpr uint64_t kWaitLimitNs = MXFP4_WAIT_LIMIT_NS;
+
+// Test-only builds (compiled with MXFP4_TEST_WITHHOLD_STAGE, never the
+// product library): the producer of CTA 0 withholds its first weight stage
+// (no copy, no arrive), so the consumers' bounded wait on it runs out. This
+// exercises the timeout path - status word, wind-down, a usable context -
+// without any fault.
+__device__ __forceinline__ bool withhold_stage(uint32_t index) {
+#ifdef MXFP4_TEST_WITHHOLD_STAGE
+    return blockIdx.x == 0 && index == 0;
+#else
+    (void)index;
+    return false;
+#endif
+}
 
 // Bits of the per-device status word.
 constexpr unsigned kStatusTimeout = 1u;

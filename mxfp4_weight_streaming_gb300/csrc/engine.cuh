@@ -583,6 +583,10 @@ __device__ void producer_role(const typename P::Params& p, const Smem& S, const 
             // been consumed, so a consumer that sees this tag can wait on the
             // slot's full barrier without mistaking an older phase for it.
             sts_u32_volatile(bars.ring_tag(slot), staged);
+            if (withhold_stage(staged)) {  // test-only builds
+                ++staged;
+                continue;
+            }
             mbar_arrive_expect_tx(bars.full(slot), stage_bytes);
             // Stage layout: [box][step][16 rows][128 B], 128-byte swizzle.
             const uint32_t sbase = S.base + L.ring + slot * stage_bytes;

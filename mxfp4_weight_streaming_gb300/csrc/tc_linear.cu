@@ -91,8 +91,9 @@ struct Cfg {
     static constexpr int kOffB = NA * kSlotA;
     static constexpr int kOffBars = kOffB + NG * kSlotB;
     // mbarriers: fullA, emptyA, sfaReady [NA]; fullB, emptyB, sfbReady [NG];
-    // accFull, accEmpty, inbox; then the abort flag and the TMEM base word.
-    static constexpr int kNumBars = 3 * NA + 3 * NG + 3;
+    // accFull, accEmpty, inbox, drain; then the abort flag and the TMEM base
+    // word.
+    static constexpr int kNumBars = 3 * NA + 3 * NG + 4;
     static constexpr int kOffAbort = kOffBars + 8 * kNumBars;
     static constexpr int kOffTmemSlot = kOffAbort + 4;
     static constexpr int kOffInbox = (kOffTmemSlot + 4 + 127) / 128 * 128;
@@ -121,6 +122,7 @@ struct Bars {
     __device__ uint32_t acc_full() const { return base + 8 * (3 * na + 3 * nb); }
     __device__ uint32_t acc_empty() const { return base + 8 * (3 * na + 3 * nb + 1); }
     __device__ uint32_t inbox() const { return base + 8 * (3 * na + 3 * nb + 2); }
+    __device__ uint32_t drain() const { return base + 8 * (3 * na + 3 * nb + 3); }
 };
 
 // The CTA's share: tiles [tile0, tile0 + ntile) in batches (sizes as even
@@ -166,6 +168,11 @@ __device__ void producer(const TcLinearParams& p, const CUtensorMap* amap, const
                     break;
                 }
                 const uint32_t slot = base + C::kOffA + r.slot * C::kSlotA;
+                if (withhold_stage(static_cast<uint32_t>(issued))) {  // test-only builds
+                    ++issued;
+                    r.next(NA);
+                    continue;
+                }
                 mbar_arrive_expect_tx(bars.full_a(r.slot), static_cast<uint32_t>(SA * kAtomPackedA));
                 tma_load_3d_tc(slot, amap, 0, (t0 + ti) * kTileRows, atom0, bars.full_a(r.slot), policy);
                 ++issued;
@@ -189,7 +196,7 @@ __device__ void producer(const TcLinearParams& p, const CUtensorMap* amap, const
 // offsets (the start-address field of a descriptor is the byte address / 16
 // in its low bits, so an offset inside a buffer is a plain add).
 template <class C, int NPAD, int SA, int NA, int NG>
-__device__ void mma_issuer(const Work& w, uint32_t base, uint32_t tbase, const Bars& bars, const WaitCtx& wc) {
+__device__ bool mma_issue_all(const Work& w, uint32_t base, uint32_t tbase, const Bars& bars, const WaitCtx& wc) {
     uint64_t adesc[NA], bdesc[NG];
 #pragma unroll
     for (int s = 0; s < NA; ++s) adesc[s] = operand_desc(base + C::kOffA + s * C::kSlotA);
@@ -198,19 +205,19 @@ __device__ void mma_issuer(const Work& w, uint32_t base, uint32_t tbase, const B
     Ring ra, rb;
     for (int b = 0; b < w.nbatch; ++b) {
         const int bt = w.batch_size(b);
-        if (!mbar_wait(bars.acc_empty(), (static_cast<uint32_t>(b) & 1u) ^ 1u, wc)) return;
+        if (!mbar_wait(bars.acc_empty(), (static_cast<uint32_t>(b) & 1u) ^ 1u, wc)) return false;
         for (int k = 0; k < w.spt; ++k) {
             const int off = ((w.st0 + k) * SA) & 3;  // the stage's first atom within its 4-atom scale group
-            if (!mbar_wait(bars.full_b(rb.slot), rb.phase, wc)) return;
-            if (!mbar_wait(bars.sfb_ready(rb.slot), rb.phase, wc)) return;
+            if (!mbar_wait(bars.full_b(rb.slot), rb.phase, wc)) return false;
+            if (!mbar_wait(bars.sfb_ready(rb.slot), rb.phase, wc)) return false;
             uint64_t bd = 0;
 #pragma unroll
             for (int s = 0; s < NG; ++s)
                 if (s == rb.slot) bd = bdesc[s];
             const uint32_t sfb = tbase + C::kSfbCol + rb.slot * 16;
             for (int ti = 0; ti < bt; ++ti) {
-                if (!mbar_wait(bars.full_a(ra.slot), ra.phase, wc)) return;
-                if (!mbar_wait(bars.sfa_ready(ra.slot), ra.phase, wc)) return;
+                if (!mbar_wait(bars.full_a(ra.slot), ra.phase, wc)) return false;
+                if (!mbar_wait(bars.sfa_ready(ra.slot), ra.phase, wc)) return false;
                 fence_after_sync();
                 uint64_t ad = 0;
 #pragma unroll
@@ -235,6 +242,19 @@ __device__ void mma_issuer(const Work& w, uint32_t base, uint32_t tbase, const B
         }
         commit_to(bars.acc_full());
     }
+    return true;
+}
+
+template <class C, int NPAD, int SA, int NA, int NG>
+__device__ void mma_issuer(const Work& w, uint32_t base, uint32_t tbase, const Bars& bars, const WaitCtx& wc) {
+    if (mma_issue_all<C, NPAD, SA, NA, NG>(w, base, tbase, bars, wc)) return;
+    // Aborted: MMAs issued so far may still read shared memory and write
+    // TMEM. One more commit tracks them all; wait for it (bounded, whatever
+    // the abort flag says) before the CTA frees TMEM and exits.
+    commit_to(bars.drain());
+    int never = 0;
+    const WaitCtx own{wc.status, &never};
+    mbar_wait(bars.drain(), 0, own);
 }
 
 // ------------------------------------------------------------ converter
@@ -551,6 +571,7 @@ __global__ void __launch_bounds__(Cfg<NPAD, SA, NA, NG, W>::kThreads, 1)
         mbar_init(bars.acc_full(), 1);
         mbar_init(bars.acc_empty(), kEpilogueWarps);
         mbar_init(bars.inbox(), static_cast<uint32_t>((p.cl > 1 ? p.cl - 1 : 1) * kEpilogueWarps));
+        mbar_init(bars.drain(), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }

@@ -35,6 +35,22 @@ def test_every_declared_symbol_is_exported(L):
         assert hasattr(L, name), name
 
 
+def test_only_the_c_abi_is_exported(L):
+    """Every other symbol is private to the library: a process that loads two
+    builds (a test variant beside the product) must not merge their launch
+    caches, which gcc would otherwise emit as process-wide unique objects."""
+    import shutil
+    import subprocess
+    import mxfp4_weight_streaming_gb300 as mx
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", mx.LIB_PATH], capture_output=True, text=True, check=True).stdout
+    exported = sorted(line.split()[-1] for line in out.splitlines() if line.strip())
+    assert exported == declared_functions()
+    assert not [line for line in out.splitlines() if " u " in line]
+
+
 def test_strerror(L):
     import mxfp4_weight_streaming_gb300 as mx
     for code in range(7):

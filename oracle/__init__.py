@@ -50,7 +50,8 @@ def _bind(L):
     L.oracle_route.restype = None
     L.oracle_route.argtypes = [P, I64, I64, ctypes.c_int, P, P]
     L.oracle_moe.restype = ctypes.c_int
-    L.oracle_moe.argtypes = [P, I64, I64, P, I64, ctypes.c_int, P, P, P, P, I64, P, I64, P, I64, P, P]
+    L.oracle_moe.argtypes = [P, I64, I64, P, I64, ctypes.c_int, ctypes.c_int, P, P, P, P, I64, P, I64, P, I64,
+                              P, P]
     return L
 
 
@@ -138,18 +139,20 @@ class Oracle:
         return ids, g
 
     def moe(self, x, logits: np.ndarray, top_k: int, w1: dict, w2: dict, inter: int,
-            tok: np.ndarray | None = None, cols: np.ndarray | None = None):
+            tok: np.ndarray | None = None, cols: np.ndarray | None = None, n_shared: int = 0):
         """Grouped top-k MoE in float64.
 
         ``w1``/``w2`` map expert id -> (wq, ws) packed arrays (only experts
-        that the selected tokens route to are needed). Returns (y, rss)
+        that the selected tokens route to are needed). With ``n_shared`` > 0,
+        experts e .. e + n_shared - 1 (e = the logits' width) are shared
+        experts that every token applies with weight 1. Returns (y, rss)
         float64 [ntok, ncols].
         """
         xb = _bf16_bits(x)
         t, hidden = xb.shape
         lg = np.ascontiguousarray(logits, dtype=np.float32)
         e = lg.shape[1]
-        arr = ctypes.c_void_p * e
+        arr = ctypes.c_void_p * max([e + n_shared] + [ex + 1 for ex in list(w1) + list(w2)])
         keep = []
 
         def table(d, idx):
@@ -169,7 +172,7 @@ class Oracle:
         ncols = hidden if cols is None else cols.size
         y = np.empty((ntok, ncols), np.float64)
         rss = np.empty((ntok, ncols), np.float64)
-        rc = self.L.oracle_moe(_ptr(xb), t, hidden, _ptr(lg), e, top_k, p1q, p1s, p2q, p2s, inter,
+        rc = self.L.oracle_moe(_ptr(xb), t, hidden, _ptr(lg), e, top_k, n_shared, p1q, p1s, p2q, p2s, inter,
                                _ptr(tok), ntok, _ptr(cols), ncols, _ptr(y), _ptr(rss))
         if rc != 0:
             raise ValueError("oracle_moe: a routed expert's weights were not provided")
@@ -203,8 +206,8 @@ def route(logits, top_k):
     return default().route(logits, top_k)
 
 
-def moe(x, logits, top_k, w1, w2, inter, tok=None, cols=None):
-    return default().moe(x, logits, top_k, w1, w2, inter, tok, cols)
+def moe(x, logits, top_k, w1, w2, inter, tok=None, cols=None, n_shared=0):
+    return default().moe(x, logits, top_k, w1, w2, inter, tok, cols, n_shared)
 
 
 def within_tolerance(y_gpu: np.ndarray, y_ref: np.ndarray, rss: np.ndarray,

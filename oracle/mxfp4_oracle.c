@@ -216,26 +216,36 @@ void oracle_route(const float* logits, int64_t t, int64_t e, int top_k, int32_t*
  *     h = SiLU(a) * b with SiLU(z) = z / (1 + exp(-z)),
  *     o = W2_e . h
  *   y[t] = sum over the selected experts, in selection order, of g * o.
+ * Shared experts ([Z] Quantization: a token uses its top-k routed experts
+ * plus the layer's shared experts, e.g. 8 routed and 1 shared of 257): the
+ * tables hold n_shared more experts, e .. e + n_shared - 1, which every
+ * token applies after its routed ones with weight g = 1 (the pages print no
+ * weight for them; 1 is the plain reading of "uses").
  * rss[t][n] = sqrt(sum over (e, j) of (g * h_j * w2_e[n, j])^2).
  * Per-expert pointers (w1q[e], ...) may be NULL for experts no selected
  * token routes to. Tokens and output columns may be subsets (tok / cols
  * NULL selects all); y and rss are [ntok][ncols]. Returns 0, or -1 if a
  * needed expert is missing. */
 int oracle_moe(const uint16_t* x, int64_t t, int64_t hidden, const float* logits, int64_t e, int top_k,
-               const uint8_t* const* w1q, const uint8_t* const* w1s, const uint8_t* const* w2q,
+               int n_shared, const uint8_t* const* w1q, const uint8_t* const* w1s, const uint8_t* const* w2q,
                const uint8_t* const* w2s, int64_t inter, const int64_t* tok, int64_t ntok,
                const int64_t* cols, int64_t ncols, double* y, double* rss) {
     (void)t;
-    int64_t npair = ntok * top_k;
+    int kp = top_k + n_shared; /* pairs per token */
+    int64_t npair = ntok * kp;
     int32_t* ids = (int32_t*)malloc(sizeof(int32_t) * (size_t)npair);
     double* g = (double*)malloc(sizeof(double) * (size_t)npair);
     double* h = (double*)malloc(sizeof(double) * (size_t)(npair * inter));
     int missing = 0;
     for (int64_t i = 0; i < ntok; i++) {
         int64_t ti = tok ? tok[i] : i;
-        route_one(logits + ti * e, e, top_k, ids + i * top_k, g + i * top_k);
-        for (int j = 0; j < top_k; j++) {
-            int ex = ids[i * top_k + j];
+        route_one(logits + ti * e, e, top_k, ids + i * kp, g + i * kp);
+        for (int s = 0; s < n_shared; s++) {
+            ids[i * kp + top_k + s] = (int32_t)(e + s);
+            g[i * kp + top_k + s] = 1.0;
+        }
+        for (int j = 0; j < kp; j++) {
+            int ex = ids[i * kp + j];
             if (!w1q[ex] || !w1s[ex] || !w2q[ex] || !w2s[ex]) missing = 1;
         }
     }
@@ -247,7 +257,7 @@ int oracle_moe(const uint16_t* x, int64_t t, int64_t hidden, const float* logits
     }
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t p = 0; p < npair; p++) {
-        int64_t i = p / top_k;
+        int64_t i = p / kp;
         int64_t ti = tok ? tok[i] : i;
         int ex = ids[p];
         const uint16_t* xt = x + ti * hidden;
@@ -267,8 +277,8 @@ int oracle_moe(const uint16_t* x, int64_t t, int64_t hidden, const float* logits
         int64_t i = q / ncols;
         int64_t col = cols ? cols[q % ncols] : (q % ncols);
         double acc = 0.0, sq = 0.0;
-        for (int j = 0; j < top_k; j++) {
-            int64_t p = i * top_k + j;
+        for (int j = 0; j < kp; j++) {
+            int64_t p = i * kp + j;
             int ex = ids[p];
             double o = 0.0;
             for (int64_t c = 0; c < inter; c++) {

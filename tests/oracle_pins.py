@@ -291,6 +291,38 @@ def check_moe_top1(orc, pin):
         assert np.allclose(y[ti], ref, rtol=1e-10, atol=1e-12 * np.abs(W2) @ np.abs(h)), ti
 
 
+def check_moe_shared(orc, pin):
+    """Two shared experts after the routed top-2: each adds its own SwiGLU
+    FFN output with weight 1 ("Zyphra Inference Wave 2", section
+    "Quantization": a token uses its top-k routed experts plus the layer's
+    shared experts)."""
+    from scipy.special import expit, softmax
+    rng = np.random.default_rng(31)
+    e, ns, hidden, inter, t, top_k = 5, 2, 64, 32, 4, 2
+    w1 = {ex: _pack(rng, 2 * inter, hidden) for ex in range(e + ns)}
+    w2 = {ex: _pack(rng, hidden, inter) for ex in range(e + ns)}
+    x = bf16_round(rng.normal(0, 1, (t, hidden)))
+    lg = rng.normal(0, 1, (t, e)).astype(np.float32)
+    y, _ = orc.moe(x, lg, top_k, w1, w2, inter, n_shared=ns)
+    xs = x.float().double().numpy()
+
+    def ffn(ex, xt):
+        W1 = lib_decode(pin, *w1[ex])
+        a, b = W1[:inter] @ xt, W1[inter:] @ xt
+        return lib_decode(pin, *w2[ex]) @ (a * expit(a) * b)
+
+    for ti in range(t):
+        order = sorted(range(e), key=lambda c: (-float(lg[ti, c]), c))[:top_k]
+        g = softmax(lg[ti, order].astype(np.float64))
+        ref = sum(gi * ffn(ex, xs[ti]) for gi, ex in zip(g, order)) + sum(ffn(e + s, xs[ti]) for s in range(ns))
+        mag = sum(np.abs(ffn(ex, xs[ti])) for ex in range(e + ns))
+        assert np.allclose(y[ti], ref, rtol=1e-10, atol=1e-12 * float(mag.max())), ti
+    # With no shared expert the call is the routed MoE itself.
+    y0, _ = orc.moe(x, lg, top_k, w1, w2, inter)
+    y0s, _ = orc.moe(x, lg, top_k, w1, w2, inter, n_shared=0)
+    assert np.array_equal(y0, y0s)
+
+
 def check_moe_mpmath(orc, pin):
     import mpmath
     mpmath.mp.dps = 40
@@ -341,6 +373,7 @@ ALL_CHECKS = [
     ("route", check_route, False),
     ("moe_top1", check_moe_top1, True),
     ("moe_mpmath", check_moe_mpmath, True),
+    ("moe_shared", check_moe_shared, True),
 ]
 
 

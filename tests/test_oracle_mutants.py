@@ -36,6 +36,9 @@ MUTANTS = [
      "double silu = b / (1.0 + exp(-b));\n            h[p * inter + r] = silu * a;"),
     ("SiLU sign error", "double silu = a / (1.0 + exp(-a));", "double silu = a / (1.0 + exp(a));"),
     ("gate weight dropped", "acc += g[p] * o;", "acc += o;"),
+    ("shared expert weight halved", "g[i * kp + top_k + s] = 1.0;", "g[i * kp + top_k + s] = 0.5;"),
+    ("shared expert index off by one", "ids[i * kp + top_k + s] = (int32_t)(e + s);",
+     "ids[i * kp + top_k + s] = (int32_t)(e + s - 1);"),
     ("W2 operand transposed", "dequant_at(w2q[ex], w2s[ex], inter, col, c)", "dequant_at(w2q[ex], w2s[ex], inter, c % (col + 1), col % inter)"),
 ]
 

@@ -66,6 +66,10 @@ def load() -> ctypes.CDLL:
     L.mxfp4_moe_workspace_size.argtypes = [I64, I64, I, I64, I64]
     L.mxfp4_moe.restype = I
     L.mxfp4_moe.argtypes = [P, I64, I64, P, I64, I, P, P, P, P, I64, P, P, P, P, ctypes.c_size_t, P]
+    L.mxfp4_moe_shared_workspace_size.restype = ctypes.c_size_t
+    L.mxfp4_moe_shared_workspace_size.argtypes = [I64, I64, I, I, I64, I64]
+    L.mxfp4_moe_shared.restype = I
+    L.mxfp4_moe_shared.argtypes = [P, I64, I64, P, I64, I, I, P, P, P, P, I64, P, P, P, P, ctypes.c_size_t, P]
     L.mxfp4_last_device_status.restype = I
     L.mxfp4_last_device_status.argtypes = [P]
     L.mxfp4_linear_plan.restype = I
@@ -109,6 +113,16 @@ def mxfp4_moe(x_ptr, t, hidden, logits_ptr, e, top_k, w1q, w1s, w2q, w2s, inter,
                             gw_ptr, ws_ptr, ws_bytes, stream_ptr)
 
 
+def mxfp4_moe_shared_workspace_size(t, e, top_k, n_shared, hidden, inter) -> int:
+    return load().mxfp4_moe_shared_workspace_size(t, e, top_k, n_shared, hidden, inter)
+
+
+def mxfp4_moe_shared(x_ptr, t, hidden, logits_ptr, e, top_k, n_shared, w1q, w1s, w2q, w2s, inter, y_ptr, ids_ptr,
+                     gw_ptr, ws_ptr, ws_bytes, stream_ptr) -> int:
+    return load().mxfp4_moe_shared(x_ptr, t, hidden, logits_ptr, e, top_k, n_shared, w1q, w1s, w2q, w2s, inter,
+                                   y_ptr, ids_ptr, gw_ptr, ws_ptr, ws_bytes, stream_ptr)
+
+
 def mxfp4_last_device_status(stream_ptr) -> int:
     return load().mxfp4_last_device_status(stream_ptr)
 
@@ -137,30 +151,38 @@ def linear(x, wq, ws, out=None, stream=None):
     return y
 
 
-def moe_workspace(t, e, top_k, hidden, inter, device):
+def moe_workspace(t, e, top_k, hidden, inter, device, n_shared=0):
     import torch
-    nbytes = mxfp4_moe_workspace_size(t, e, top_k, hidden, inter)
+    nbytes = mxfp4_moe_shared_workspace_size(t, e, top_k, n_shared, hidden, inter)
     return torch.empty(nbytes, dtype=torch.uint8, device=device)
 
 
-def moe(x, logits, top_k, w1q, w1s, w2q, w2s, workspace=None, out=None, topk_ids=None, topk_w=None, stream=None):
+def moe(x, logits, top_k, w1q, w1s, w2q, w2s, workspace=None, out=None, topk_ids=None, topk_w=None, stream=None,
+        n_shared=0):
     """Grouped top-k MoE: x bf16 [t, hidden], logits f32 [t, e] -> bf16 [t, hidden].
 
-    w1q/w1s: [e, 2*inter, hidden/2] / [e, 2*inter, hidden/32] (gate rows first);
-    w2q/w2s: [e, hidden, inter/2] / [e, hidden, inter/32].
+    w1q/w1s: [e + n_shared, 2*inter, hidden/2] / [.., hidden/32] (gate rows first);
+    w2q/w2s: [e + n_shared, hidden, inter/2] / [.., inter/32]. Experts e ..
+    e + n_shared - 1 are shared experts every token applies with weight 1
+    (mxfp4_moe_shared); n_shared = 0 calls mxfp4_moe.
     """
     import torch
     t, hidden = x.shape
     e = logits.shape[1]
     inter = w2q.shape[2] * 2
     if workspace is None:
-        workspace = moe_workspace(t, e, top_k, hidden, inter, x.device)
+        workspace = moe_workspace(t, e, top_k, hidden, inter, x.device, n_shared)
     y = out if out is not None else torch.empty((t, hidden), dtype=torch.bfloat16, device=x.device)
     ids_ptr = topk_ids.data_ptr() if topk_ids is not None else None
     gw_ptr = topk_w.data_ptr() if topk_w is not None else None
-    _check(mxfp4_moe(x.data_ptr(), t, hidden, logits.data_ptr(), e, top_k, w1q.data_ptr(), w1s.data_ptr(),
-                     w2q.data_ptr(), w2s.data_ptr(), inter, y.data_ptr(), ids_ptr, gw_ptr, workspace.data_ptr(),
-                     workspace.numel(), _stream(stream)), "mxfp4_moe")
+    if n_shared:
+        _check(mxfp4_moe_shared(x.data_ptr(), t, hidden, logits.data_ptr(), e, top_k, n_shared, w1q.data_ptr(),
+                                w1s.data_ptr(), w2q.data_ptr(), w2s.data_ptr(), inter, y.data_ptr(), ids_ptr, gw_ptr,
+                                workspace.data_ptr(), workspace.numel(), _stream(stream)), "mxfp4_moe_shared")
+    else:
+        _check(mxfp4_moe(x.data_ptr(), t, hidden, logits.data_ptr(), e, top_k, w1q.data_ptr(), w1s.data_ptr(),
+                         w2q.data_ptr(), w2s.data_ptr(), inter, y.data_ptr(), ids_ptr, gw_ptr, workspace.data_ptr(),
+                         workspace.numel(), _stream(stream)), "mxfp4_moe")
     return y
 
 

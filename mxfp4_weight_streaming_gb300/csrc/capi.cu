@@ -298,22 +298,36 @@ size_t mxfp4_moe_workspace_size(int64_t t, int64_t e, int top_k, int64_t hidden,
     return mxfp4::moe_workspace_bytes(t, e, top_k, hidden, inter);
 }
 
-int mxfp4_moe(const void* x, int64_t t, int64_t hidden, const float* router_logits, int64_t e, int top_k,
-              const uint8_t* w1q, const uint8_t* w1s, const uint8_t* w2q, const uint8_t* w2s, int64_t inter, void* y,
-              int32_t* topk_ids, float* topk_w, void* workspace, size_t workspace_bytes, void* stream) {
+size_t mxfp4_moe_shared_workspace_size(int64_t t, int64_t e, int top_k, int n_shared, int64_t hidden,
+                                       int64_t inter) {
+    if (t <= 0 || e <= 0 || top_k <= 0 || n_shared < 0 || hidden <= 0 || inter <= 0) return 0;
+    return mxfp4::moe_workspace_bytes(t, e, top_k + n_shared, hidden, inter);
+}
+
+}  // extern "C"
+
+namespace {
+
+int moe_call(const void* x, int64_t t, int64_t hidden, const float* router_logits, int64_t e, int top_k,
+             int n_shared, const uint8_t* w1q, const uint8_t* w1s, const uint8_t* w2q, const uint8_t* w2s,
+             int64_t inter, void* y, int32_t* topk_ids, float* topk_w, void* workspace, size_t workspace_bytes,
+             void* stream) {
     if (!x || !router_logits || !w1q || !w1s || !w2q || !w2s || !y || t <= 0 || hidden <= 0 || e <= 0 ||
-        top_k <= 0 || inter <= 0)
+        top_k <= 0 || inter <= 0 || n_shared < 0)
         return MXFP4_ERR_INVALID_ARG;
-    if (hidden % 32 != 0 || inter % 32 != 0 || t > 256 || e > 1024 || top_k > 16 || top_k > e)
+    const int64_t et = e + n_shared;  // experts in the weight arrays
+    if (hidden % 32 != 0 || inter % 32 != 0 || t > 256 || e > 1024 || top_k > 16 || top_k > e ||
+        n_shared > 16 || et > 1024)
         return MXFP4_ERR_SHAPE;
-    if (e * 2 * inter >= (int64_t(1) << 31) || e * hidden >= (int64_t(1) << 31)) return MXFP4_ERR_SHAPE;
+    if (et * 2 * inter >= (int64_t(1) << 31) || et * hidden >= (int64_t(1) << 31)) return MXFP4_ERR_SHAPE;
     if (!aligned(x, 16) || !aligned(w1q, 16) || !aligned(w1s, 16) || !aligned(w2q, 16) || !aligned(w2s, 16) ||
         !aligned(y, 2) || !aligned(router_logits, 4) || (topk_ids && !aligned(topk_ids, 4)) ||
         (topk_w && !aligned(topk_w, 4)))
         return MXFP4_ERR_ALIGN;
     if (!workspace) return MXFP4_ERR_WORKSPACE;
     if (!aligned(workspace, 256)) return MXFP4_ERR_ALIGN;
-    if (workspace_bytes < mxfp4::moe_workspace_bytes(t, e, top_k, hidden, inter)) return MXFP4_ERR_WORKSPACE;
+    if (workspace_bytes < mxfp4::moe_workspace_bytes(t, e, top_k + n_shared, hidden, inter))
+        return MXFP4_ERR_WORKSPACE;
     DeviceInfo* d = nullptr;
     if (int rc = device_info(&d)) return rc;
     mxfp4::MoeArgs a{};
@@ -333,7 +347,27 @@ int mxfp4_moe(const void* x, int64_t t, int64_t hidden, const float* router_logi
     a.top_k = top_k;
     a.hidden = static_cast<int>(hidden);
     a.inter = static_cast<int>(inter);
+    a.n_shared = n_shared;
     return mxfp4::launch_moe(w1q, w2q, a, d->num_sms, d->max_smem, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int mxfp4_moe(const void* x, int64_t t, int64_t hidden, const float* router_logits, int64_t e, int top_k,
+              const uint8_t* w1q, const uint8_t* w1s, const uint8_t* w2q, const uint8_t* w2s, int64_t inter, void* y,
+              int32_t* topk_ids, float* topk_w, void* workspace, size_t workspace_bytes, void* stream) {
+    return moe_call(x, t, hidden, router_logits, e, top_k, 0, w1q, w1s, w2q, w2s, inter, y, topk_ids, topk_w,
+                    workspace, workspace_bytes, stream);
+}
+
+int mxfp4_moe_shared(const void* x, int64_t t, int64_t hidden, const float* router_logits, int64_t e, int top_k,
+                     int n_shared, const uint8_t* w1q, const uint8_t* w1s, const uint8_t* w2q, const uint8_t* w2s,
+                     int64_t inter, void* y, int32_t* topk_ids, float* topk_w, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+    return moe_call(x, t, hidden, router_logits, e, top_k, n_shared, w1q, w1s, w2q, w2s, inter, y, topk_ids,
+                    topk_w, workspace, workspace_bytes, stream);
 }
 
 int mxfp4_last_device_status(void* stream) {

@@ -7,6 +7,12 @@
 //   g_t   = softmax over the selected logits,
 //   h     = SiLU(W1_gate x_t) * (W1_up x_t)         (per routed pair, fp32)
 //   y_t   = bf16( sum_j g_tj * W2_{ids_tj} h_tj )   (selection order)
+// With shared experts ("Zyphra Inference Wave 2", section "Quantization": a
+// token uses its top-k routed experts plus the layer's shared experts) the
+// weight arrays hold n_shared more experts after the E routed ones. Every
+// token applies each of them after its routed experts, with g = 1: they are
+// n_shared more (token, slot) pairs per token, and from the counting sort on
+// nothing distinguishes them from routed pairs.
 //
 // Four launches on the caller's stream:
 //   1. route   : one CTA. Top-k + softmax per token (a warp per token), then
@@ -44,7 +50,7 @@ constexpr int kRouteThreads = 1024;
 // Device pointers into the caller's workspace.
 struct MoeWork {
     int* header;  // [0] chunks for gate/up, [1] chunks for down
-    int* ids;     // [P] expert of pair p = t*top_k + j
+    int* ids;     // [P] expert of pair p = t*kp + j (kp = top_k + n_shared)
     float* gw;    // [P] gate weight of pair p
     int* pos;     // [P] sorted position of pair p
     int* sorted;  // [P] pair at sorted position
@@ -86,10 +92,10 @@ static MoeWork carve(void* base, int64_t P, int64_t hidden, int64_t inter, size_
     return w;
 }
 
-size_t moe_workspace_bytes(int64_t t, int64_t e, int top_k, int64_t hidden, int64_t inter) {
+size_t moe_workspace_bytes(int64_t t, int64_t e, int kp, int64_t hidden, int64_t inter) {
     (void)e;
     size_t total = 0;
-    carve(nullptr, t * top_k, hidden, inter, &total);
+    carve(nullptr, t * kp, hidden, inter, &total);
     return total;
 }
 
@@ -173,12 +179,16 @@ __device__ __forceinline__ void warp_topk(const float* row, int E, int top_k, in
     }
 }
 
+// Pairs: token t's slot j is pair t * kp + j, kp = top_k + n_shared; slots
+// j >= top_k are the shared experts E + (j - top_k) with weight 1.
 __global__ void __launch_bounds__(kRouteThreads, 1)
-    moe_route_kernel(const float* __restrict__ logits, int T, int E, int top_k, MoeWork w, int32_t* topk_ids,
-                     float* topk_w) {
+    moe_route_kernel(const float* __restrict__ logits, int T, int E, int top_k, int n_shared, MoeWork w,
+                     int32_t* topk_ids, float* topk_w) {
     extern __shared__ int route_smem[];
-    const int P = T * top_k;
-    int* s_ids = route_smem;  // [P], then two [E] tables (see below)
+    const int kp = top_k + n_shared;
+    const int P = T * kp;
+    const int Et = E + n_shared;  // experts in the weight arrays
+    int* s_ids = route_smem;  // [P], then two [Et] tables (see below)
     __shared__ int warp_tot[32];
     __shared__ int totals[3];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -203,13 +213,19 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
                 z += ex[j];
             }
             for (int j = 0; j < top_k; ++j) {
-                const int p = t * top_k + j;
+                const int p = t * kp + j;
                 const float g = ex[j] / z;
                 s_ids[p] = sel_i[j];
                 w.ids[p] = sel_i[j];
                 w.gw[p] = g;
-                if (topk_ids) topk_ids[p] = sel_i[j];
-                if (topk_w) topk_w[p] = g;
+                if (topk_ids) topk_ids[t * top_k + j] = sel_i[j];
+                if (topk_w) topk_w[t * top_k + j] = g;
+            }
+            for (int j = 0; j < n_shared; ++j) {
+                const int p = t * kp + top_k + j;
+                s_ids[p] = E + j;
+                w.ids[p] = E + j;
+                w.gw[p] = 1.0f;
             }
         }
         __syncwarp();
@@ -217,23 +233,23 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
     __syncthreads();
 
     // Counting sort by expert; within an expert, pairs keep ascending order.
-    int* s_cnt = s_ids + P;  // [E]: pairs per expert, then the expert's first position
-    int* s_run = s_cnt + E;  // [E]: pairs of the expert placed so far
-    for (int i = threadIdx.x; i < E; i += kRouteThreads) {
+    int* s_cnt = s_ids + P;   // [Et]: pairs per expert, then the expert's first position
+    int* s_run = s_cnt + Et;  // [Et]: pairs of the expert placed so far
+    for (int i = threadIdx.x; i < Et; i += kRouteThreads) {
         s_cnt[i] = 0;
         s_run[i] = 0;
     }
     __syncthreads();
     for (int q = threadIdx.x; q < P; q += kRouteThreads) atomicAdd(&s_cnt[s_ids[q]], 1);  // order-free counts
     __syncthreads();
-    const int e = threadIdx.x;
-    const int cnt = e < E ? s_cnt[e] : 0;
+    const int e = threadIdx.x;  // Et <= kRouteThreads (checked by the host)
+    const int cnt = e < Et ? s_cnt[e] : 0;
     const int off = block_exclusive_scan(cnt, warp_tot, nullptr);
     const int n1 = (cnt + kChunkGateUp - 1) / kChunkGateUp;
     const int n2 = (cnt + kChunkDown - 1) / kChunkDown;
     const int c1 = block_exclusive_scan(n1, warp_tot, &totals[0]);
     const int c2 = block_exclusive_scan(n2, warp_tot, &totals[1]);
-    if (e < E) s_cnt[e] = off;
+    if (e < Et) s_cnt[e] = off;
     __syncthreads();
     // Positions: one warp walks the pairs in ascending order, 32 at a time;
     // lanes holding the same expert are ranked by lane.
@@ -254,7 +270,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
             __syncwarp();
         }
     }
-    if (e < E && cnt > 0) {
+    if (e < Et && cnt > 0) {
         for (int q = 0; q < n1; ++q) {
             w.c1_e[c1 + q] = e;
             w.c1_start[c1 + q] = off + q * kChunkGateUp;
@@ -278,7 +294,7 @@ struct GateUpParams {
     const uint8_t* w1s;      // [E*2*inter][hidden/32]
     MoeWork w;
     unsigned* status;
-    int top_k, hidden, inter;
+    int kp, hidden, inter;  // kp: pairs per token (top_k + n_shared)
     int nblk, nkb, xcols, cl, tma3d;
     int upc;                 // units per chunk = inter / 16
     SmemLayout layout;
@@ -307,7 +323,7 @@ struct GateUpProblem {
     static constexpr bool kBulkStage = true;
     __device__ static int stage_cols(const Params& p, int q) { return p.w.c1_cnt[q]; }
     __device__ static const uint8_t* stage_row(const Params& p, int q, int col) {
-        const int token = p.w.sorted[p.w.c1_start[q] + col] / p.top_k;
+        const int token = p.w.sorted[p.w.c1_start[q] + col] / p.kp;
         return reinterpret_cast<const uint8_t*>(p.x + static_cast<size_t>(token) * p.hidden);
     }
 
@@ -408,14 +424,14 @@ struct DownProblem {
 };
 
 // ---------------------------------------------------------------- combine
-__global__ void moe_combine_kernel(MoeWork w, int T, int top_k, int hidden, __nv_bfloat16* __restrict__ y) {
+__global__ void moe_combine_kernel(MoeWork w, int T, int kp, int hidden, __nv_bfloat16* __restrict__ y) {
     const int64_t total = (int64_t)T * hidden;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
         const int t = static_cast<int>(i / hidden);
         const int n = static_cast<int>(i - (int64_t)t * hidden);
         float s = 0.f;
-        for (int j = 0; j < top_k; ++j) {
-            const int p = t * top_k + j;
+        for (int j = 0; j < kp; ++j) {
+            const int p = t * kp + j;
             s = fmaf(w.gw[p], w.o[(size_t)w.pos[p] * hidden + n], s);
         }
         y[i] = __float2bfloat16_rn(s);
@@ -425,7 +441,9 @@ __global__ void moe_combine_kernel(MoeWork w, int T, int top_k, int hidden, __nv
 // ------------------------------------------------------------------- host
 int launch_moe(const uint8_t* w1q, const uint8_t* w2q, const MoeArgs& a, int num_sms, int max_smem,
                cudaStream_t stream) {
-    const int64_t P = (int64_t)a.T * a.top_k;
+    const int kp = a.top_k + a.n_shared;
+    const int64_t P = (int64_t)a.T * kp;
+    const int64_t Et = (int64_t)a.E + a.n_shared;
     MoeWork w = carve(a.workspace, P, a.hidden, a.inter, nullptr);
 
     GateUpParams g{};
@@ -433,7 +451,7 @@ int launch_moe(const uint8_t* w1q, const uint8_t* w2q, const MoeArgs& a, int num
     g.w1s = a.w1s;
     g.w = w;
     g.status = a.status;
-    g.top_k = a.top_k;
+    g.kp = kp;
     g.hidden = a.hidden;
     g.inter = a.inter;
     g.nblk = a.hidden / 32;
@@ -469,21 +487,21 @@ int launch_moe(const uint8_t* w1q, const uint8_t* w2q, const MoeArgs& a, int num
         return MXFP4_ERR_SHAPE;
 
     CUtensorMap map1, map2;
-    if (int rc = encode_weights(&map1, w1q, (int64_t)a.E * 2 * a.inter, a.hidden, static_cast<int>(g.layout.steps),
+    if (int rc = encode_weights(&map1, w1q, Et * 2 * a.inter, a.hidden, static_cast<int>(g.layout.steps),
                                 &g.tma3d))
         return rc;
-    if (int rc = encode_weights(&map2, w2q, (int64_t)a.E * a.hidden, a.inter, static_cast<int>(d.layout.steps),
+    if (int rc = encode_weights(&map2, w2q, Et * a.hidden, a.inter, static_cast<int>(d.layout.steps),
                                 &d.tma3d))
         return rc;
 
-    const int route_smem = static_cast<int>((P + 2 * a.E) * 4);
+    const int route_smem = static_cast<int>((P + 2 * Et) * 4);
     if (route_smem > 48 * 1024) {
         if (cudaFuncSetAttribute(moe_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, route_smem) !=
             cudaSuccess)
             return MXFP4_ERR_CUDA;
     }
-    moe_route_kernel<<<1, kRouteThreads, route_smem, stream>>>(a.logits, a.T, a.E, a.top_k, w, a.topk_ids,
-                                                               a.topk_w);
+    moe_route_kernel<<<1, kRouteThreads, route_smem, stream>>>(a.logits, a.T, a.E, a.top_k, a.n_shared, w,
+                                                               a.topk_ids, a.topk_w);
     if (cudaGetLastError() != cudaSuccess) return MXFP4_ERR_CUDA;
     // The unit counts are only known on the device; launch one CTA per SM.
     if (launch_stream_kernel<GateUpProblem>(map1, g, num_sms, num_sms, stream) != cudaSuccess) return MXFP4_ERR_CUDA;
@@ -491,7 +509,7 @@ int launch_moe(const uint8_t* w1q, const uint8_t* w2q, const MoeArgs& a, int num
     const int64_t total = (int64_t)a.T * a.hidden;
     int blocks = static_cast<int>((total + 255) / 256);
     if (blocks > num_sms * 8) blocks = num_sms * 8;
-    moe_combine_kernel<<<blocks, 256, 0, stream>>>(w, a.T, a.top_k, a.hidden, a.y);
+    moe_combine_kernel<<<blocks, 256, 0, stream>>>(w, a.T, kp, a.hidden, a.y);
     return cudaGetLastError() == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
 }
 

@@ -19,9 +19,11 @@ struct MoeArgs {
     void* workspace;
     unsigned* status;
     int T, E, top_k, hidden, inter;
+    int n_shared;            // shared experts E .. E + n_shared - 1 of the weight arrays
 };
 
-size_t moe_workspace_bytes(int64_t t, int64_t e, int top_k, int64_t hidden, int64_t inter);
+// Workspace of t tokens with kp (token, slot) pairs each (top_k + n_shared).
+size_t moe_workspace_bytes(int64_t t, int64_t e, int kp, int64_t hidden, int64_t inter);
 int launch_moe(const uint8_t* w1q, const uint8_t* w2q, const MoeArgs& a, int num_sms, int max_smem,
                cudaStream_t stream);
 

@@ -85,3 +85,27 @@ def test_argument_errors_return_before_launch(L):
     bad[2] = 48  # hidden % 32
     assert mx.mxfp4_moe(*bad) == mx.MXFP4_ERR_SHAPE
     assert mx.mxfp4_moe_workspace_size(32, 256, 8, 7168, 2048) > 0
+
+
+def test_moe_shared_argument_errors_return_before_launch(L):
+    import mxfp4_weight_streaming_gb300 as mx
+    p = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+    t, hidden, e, top_k, inter = 4, 64, 8, 2, 64
+    base = [p, t, hidden, p, e, top_k, 1, p, p, p, p, inter, p, None, None, p, 1 << 30, None]
+
+    def call(**change):
+        a = list(base)
+        for i, v in change.items():
+            a[int(i[1:])] = v
+        return mx.mxfp4_moe_shared(*a)
+
+    assert call(a6=-1) == mx.MXFP4_ERR_INVALID_ARG  # n_shared < 0
+    assert call(a6=17) == mx.MXFP4_ERR_SHAPE  # n_shared > 16
+    assert call(a4=1020, a6=5) == mx.MXFP4_ERR_SHAPE  # e + n_shared > 1024
+    assert call(a15=None) == mx.MXFP4_ERR_WORKSPACE
+    need = mx.mxfp4_moe_shared_workspace_size(t, e, top_k, 1, hidden, inter)
+    assert need > mx.mxfp4_moe_workspace_size(t, e, top_k, hidden, inter)
+    assert mx.mxfp4_moe_shared_workspace_size(t, e, top_k, 0, hidden, inter) == \
+        mx.mxfp4_moe_workspace_size(t, e, top_k, hidden, inter)
+    assert call(a16=need - 1) == mx.MXFP4_ERR_WORKSPACE
+    assert mx.mxfp4_moe_shared_workspace_size(t, e, top_k, -1, hidden, inter) == 0

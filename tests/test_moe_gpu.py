@@ -62,6 +62,51 @@ def test_moe_small(t, e, top_k, hidden, inter):
     assert_within(bf16_to_f64(y), y_ref, rss, f"moe t={t} e={e} k={top_k}")
 
 
+@pytest.mark.parametrize("t,e,top_k,hidden,inter", [(64, 64, 8, 256, 128), (128, 128, 8, 256, 128),
+                                                    (256, 128, 8, 256, 128), (256, 32, 16, 128, 64),
+                                                    (64, 1024, 16, 128, 64)])
+def test_moe_larger_t(t, e, top_k, hidden, inter):
+    """Token counts up to the header's limit (t <= 256), and its largest e
+    and top_k: many experts receive more tokens than one chunk holds."""
+    seed = 1000 + t + e + top_k
+    dev, W1, W2 = _experts(seed, e, hidden, inter)
+    x = synth.tokens(seed, t, hidden, device="cuda")
+    lg = synth.logits(seed, t, e, device="cuda")
+    y, ids, gw = _run(x, lg, top_k, dev)
+    lgn = lg.cpu().numpy()
+    ids_ref, g_ref = oracle.route(lgn, top_k)
+    assert np.array_equal(ids.cpu().numpy(), ids_ref)
+    assert np.allclose(gw.cpu().numpy(), g_ref, rtol=1e-6, atol=0)
+    y_ref, rss = oracle.moe(x, lgn, top_k, W1, W2, inter)
+    assert_within(bf16_to_f64(y), y_ref, rss, f"moe t={t} e={e} k={top_k}")
+
+
+@pytest.mark.parametrize("t,e,top_k,n_shared,hidden,inter", [(8, 16, 4, 1, 256, 128), (32, 64, 8, 2, 512, 256),
+                                                             (1, 8, 1, 1, 64, 32), (256, 32, 8, 1, 128, 64)])
+def test_moe_shared_experts(t, e, top_k, n_shared, hidden, inter):
+    """mxfp4_moe_shared: the weight arrays hold e routed then n_shared shared
+    experts; every token adds each shared expert's output with weight 1."""
+    mx = lib()
+    seed = 500 + t + e + n_shared
+    dev, W1, W2 = _experts(seed, e + n_shared, hidden, inter)
+    x = synth.tokens(seed, t, hidden, device="cuda")
+    lg = synth.logits(seed, t, e, device="cuda")
+    ids = Guarded((t, top_k), torch.int32)
+    gw = Guarded((t, top_k), torch.float32)
+    y = Guarded((t, hidden), torch.bfloat16)
+    ws = Guarded((mx.mxfp4_moe_shared_workspace_size(t, e, top_k, n_shared, hidden, inter),), torch.uint8)
+    mx.moe(x, lg, top_k, *dev, workspace=ws.t, out=y.t, topk_ids=ids.t, topk_w=gw.t, n_shared=n_shared)
+    for buf, name in ((ids, "topk_ids"), (gw, "topk_w"), (y, "y"), (ws, "workspace")):
+        buf.check(f"moe_shared t={t} e={e} n_shared={n_shared}: {name}")
+    lgn = lg.cpu().numpy()
+    ids_ref, g_ref = oracle.route(lgn, top_k)
+    assert np.array_equal(ids.t.cpu().numpy(), ids_ref)
+    assert np.allclose(gw.t.cpu().numpy(), g_ref, rtol=1e-6, atol=0)
+    y_ref, rss = oracle.moe(x, lgn, top_k, W1, W2, inter, n_shared=n_shared)
+    assert_within(bf16_to_f64(y.t), y_ref, rss, f"moe_shared t={t} e={e} n_shared={n_shared}")
+    assert mx.last_device_status() == mx.MXFP4_OK
+
+
 def test_moe_routing_ties_and_hot_expert():
     """Equal logits (ties to smaller index) and every token on the same
     experts: one expert gets all 32 tokens (several chunks)."""

@@ -197,6 +197,39 @@ int mxfp4_moe_shared(const void* x, int64_t t, int64_t hidden, const float* rout
                      size_t workspace_bytes, void* stream);
 
 /*
+ * Bytes of device workspace mxfp4_ffn needs for t tokens (hidden unused).
+ */
+size_t mxfp4_ffn_workspace_size(int64_t t, int64_t hidden, int64_t inter);
+
+/*
+ * Fused dense FFN chain, up -> SwiGLU -> down, in ONE persistent kernel
+ * launch (lithosai "Low-Latency Inference on AMD MI355X" and AMD
+ * "megakernel-intro", section "1. Megakernels": a layer's stages in one
+ * kernel, SMs that finish a stage early preloading the next stage's
+ * weights). The arithmetic is one SwiGLU expert of mxfp4_moe applied to
+ * every token with weight 1. For each token t:
+ *   a = W1[0:inter] x_t (gate rows), b = W1[inter:2*inter] x_t (up rows),
+ *   h = SiLU(a) * b (fp32, in the workspace), y[t] = bf16( W2 h ).
+ *   x              device bf16 [t, hidden], 16-byte aligned; 1 <= t <= 8
+ *   hidden, inter  multiples of 32, at most 2^20 (MXFP4_ERR_SHAPE also when
+ *                  the staged activations of one phase do not fit on chip)
+ *   w1q, w1s       device uint8 [2*inter, hidden/2], [2*inter, hidden/32]
+ *                  (gate rows first), 16-byte aligned
+ *   w2q, w2s       device uint8 [hidden, inter/2], [hidden, inter/32],
+ *                  16-byte aligned
+ *   y              device bf16 [t, hidden] (output)
+ *   workspace      device scratch of at least mxfp4_ffn_workspace_size()
+ *                  bytes, 256-byte aligned; contents on entry do not matter.
+ * The kernel is a cooperative launch: every CTA waits (bounded) for the
+ * gate/up results of all the others, so the whole grid must be resident. A
+ * call that shares the GPU with other work that holds SMs may therefore end
+ * in MXFP4_ERR_TIMEOUT (reported as for every call) instead of a result.
+ * The call enqueues a 4-byte memset of the workspace before the kernel.
+ */
+int mxfp4_ffn(const void* x, int64_t t, int64_t hidden, const uint8_t* w1q, const uint8_t* w1s, const uint8_t* w2q,
+              const uint8_t* w2s, int64_t inter, void* y, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Capacity in bytes of the scratch array built into the library for
  * mxfp4_moe_noalloc (held on every GPU that loads the library).
  */

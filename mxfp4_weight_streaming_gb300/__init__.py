@@ -70,6 +70,10 @@ def load() -> ctypes.CDLL:
     L.mxfp4_moe_shared_workspace_size.argtypes = [I64, I64, I, I, I64, I64]
     L.mxfp4_moe_shared.restype = I
     L.mxfp4_moe_shared.argtypes = [P, I64, I64, P, I64, I, I, P, P, P, P, I64, P, P, P, P, ctypes.c_size_t, P]
+    L.mxfp4_ffn_workspace_size.restype = ctypes.c_size_t
+    L.mxfp4_ffn_workspace_size.argtypes = [I64, I64, I64]
+    L.mxfp4_ffn.restype = I
+    L.mxfp4_ffn.argtypes = [P, I64, I64, P, P, P, P, I64, P, P, ctypes.c_size_t, P]
     L.mxfp4_last_device_status.restype = I
     L.mxfp4_last_device_status.argtypes = [P]
     L.mxfp4_linear_plan.restype = I
@@ -121,6 +125,14 @@ def mxfp4_moe_shared(x_ptr, t, hidden, logits_ptr, e, top_k, n_shared, w1q, w1s,
                      gw_ptr, ws_ptr, ws_bytes, stream_ptr) -> int:
     return load().mxfp4_moe_shared(x_ptr, t, hidden, logits_ptr, e, top_k, n_shared, w1q, w1s, w2q, w2s, inter,
                                    y_ptr, ids_ptr, gw_ptr, ws_ptr, ws_bytes, stream_ptr)
+
+
+def mxfp4_ffn_workspace_size(t, hidden, inter) -> int:
+    return load().mxfp4_ffn_workspace_size(t, hidden, inter)
+
+
+def mxfp4_ffn(x_ptr, t, hidden, w1q, w1s, w2q, w2s, inter, y_ptr, ws_ptr, ws_bytes, stream_ptr) -> int:
+    return load().mxfp4_ffn(x_ptr, t, hidden, w1q, w1s, w2q, w2s, inter, y_ptr, ws_ptr, ws_bytes, stream_ptr)
 
 
 def mxfp4_last_device_status(stream_ptr) -> int:
@@ -183,6 +195,24 @@ def moe(x, logits, top_k, w1q, w1s, w2q, w2s, workspace=None, out=None, topk_ids
         _check(mxfp4_moe(x.data_ptr(), t, hidden, logits.data_ptr(), e, top_k, w1q.data_ptr(), w1s.data_ptr(),
                          w2q.data_ptr(), w2s.data_ptr(), inter, y.data_ptr(), ids_ptr, gw_ptr, workspace.data_ptr(),
                          workspace.numel(), _stream(stream)), "mxfp4_moe")
+    return y
+
+
+def ffn(x, w1q, w1s, w2q, w2s, workspace=None, out=None, stream=None):
+    """Fused dense FFN chain: bf16 x [t, hidden] -> bf16 W2 (SiLU(W1_gate x) * (W1_up x)) [t, hidden].
+
+    w1q/w1s: [2*inter, hidden/2] / [2*inter, hidden/32] (gate rows first);
+    w2q/w2s: [hidden, inter/2] / [hidden, inter/32].
+    """
+    import torch
+    assert x.is_cuda and x.dtype == torch.bfloat16 and x.dim() == 2 and x.is_contiguous()
+    t, hidden = x.shape
+    inter = w2q.shape[1] * 2
+    if workspace is None:
+        workspace = torch.empty(mxfp4_ffn_workspace_size(t, hidden, inter), dtype=torch.uint8, device=x.device)
+    y = out if out is not None else torch.empty((t, hidden), dtype=torch.bfloat16, device=x.device)
+    _check(mxfp4_ffn(x.data_ptr(), t, hidden, w1q.data_ptr(), w1s.data_ptr(), w2q.data_ptr(), w2s.data_ptr(), inter,
+                     y.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream(stream)), "mxfp4_ffn")
     return y
 
 

@@ -10,6 +10,7 @@
 
 #include "device_common.cuh"
 #include "linear_launch.h"
+#include "ffn_launch.h"
 #include "moe_launch.h"
 #include "tc_linear_launch.h"
 #include "mxfp4.h"
@@ -368,6 +369,44 @@ int mxfp4_moe_shared(const void* x, int64_t t, int64_t hidden, const float* rout
                      size_t workspace_bytes, void* stream) {
     return moe_call(x, t, hidden, router_logits, e, top_k, n_shared, w1q, w1s, w2q, w2s, inter, y, topk_ids,
                     topk_w, workspace, workspace_bytes, stream);
+}
+
+size_t mxfp4_ffn_workspace_size(int64_t t, int64_t hidden, int64_t inter) {
+    if (t <= 0 || hidden <= 0 || inter <= 0) return 0;
+    return mxfp4::ffn_workspace_bytes(t, inter);
+}
+
+int mxfp4_ffn(const void* x, int64_t t, int64_t hidden, const uint8_t* w1q, const uint8_t* w1s, const uint8_t* w2q,
+              const uint8_t* w2s, int64_t inter, void* y, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!x || !w1q || !w1s || !w2q || !w2s || !y || t <= 0 || hidden <= 0 || inter <= 0)
+        return MXFP4_ERR_INVALID_ARG;
+    if (t > 8 || hidden % 32 != 0 || inter % 32 != 0 || hidden > (1 << 20) || inter > (1 << 20))
+        return MXFP4_ERR_SHAPE;
+    if (!aligned(x, 16) || !aligned(w1q, 16) || !aligned(w1s, 16) || !aligned(w2q, 16) || !aligned(w2s, 16) ||
+        !aligned(y, 2))
+        return MXFP4_ERR_ALIGN;
+    if (!workspace) return MXFP4_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return MXFP4_ERR_ALIGN;
+    if (workspace_bytes < mxfp4::ffn_workspace_bytes(t, inter)) return MXFP4_ERR_WORKSPACE;
+    DeviceInfo* d = nullptr;
+    if (int rc = device_info(&d)) return rc;
+    mxfp4::FfnPlan plan{};
+    if (int rc = mxfp4::plan_ffn(static_cast<int>(t), static_cast<int>(hidden), static_cast<int>(inter), d->max_smem,
+                                 &plan))
+        return rc;
+    mxfp4::FfnArgs a{};
+    a.x = static_cast<const __nv_bfloat16*>(x);
+    a.w1q = w1q;
+    a.w1s = w1s;
+    a.w2q = w2q;
+    a.w2s = w2s;
+    a.y = static_cast<__nv_bfloat16*>(y);
+    a.workspace = workspace;
+    a.status = d->status;
+    a.T = static_cast<int>(t);
+    a.hidden = static_cast<int>(hidden);
+    a.inter = static_cast<int>(inter);
+    return mxfp4::launch_ffn(a, d->num_sms, d->max_smem, static_cast<cudaStream_t>(stream));
 }
 
 int mxfp4_last_device_status(void* stream) {

@@ -48,6 +48,12 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
+// Ends an mbarrier's life so its memory may be used for anything else
+// (including a new mbarrier).
+__device__ __forceinline__ void mbar_inval(uint32_t bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void fence_barrier_init() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -99,6 +105,37 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            record_timeout(w);
+            return false;
+        }
+    }
+}
+
+// Adds v to a device word with release semantics at GPU scope: the calling
+// thread's earlier writes are visible to whoever observes the new value.
+__device__ __forceinline__ void atom_add_release_gpu(unsigned* p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Waits until the device word at p is at least want (counted by other CTAs
+// of the grid, which must all be resident). Same limits as mbar_wait.
+__device__ __forceinline__ bool wait_global_at_least(const unsigned* p, unsigned want, const WaitCtx& w) {
+    if (ld_acquire_gpu(p) >= want) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (*w.abort) return false;
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i) {
+            __nanosleep(64);
+            if (ld_acquire_gpu(p) >= want) return true;
+        }
         if (global_timer_ns() - t0 > kWaitLimitNs) {
             record_timeout(w);
             return false;

@@ -36,10 +36,19 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "device_common.cuh"
 #include "engine_layout.h"
 
 namespace mxfp4 {
+
+// Whether a problem gates its staging on inputs that other CTAs produce
+// (P::kInputGate and P::wait_inputs).
+template <class P, class = void>
+struct HasInputGate : std::false_type {};
+template <class P>
+struct HasInputGate<P, std::void_t<decltype(P::kInputGate)>> : std::bool_constant<P::kInputGate> {};
 
 // Warps of a CTA: P::NCW consumers, then the producer.
 template <class P>
@@ -777,6 +786,9 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
         const int chunk = P::chunk_of(p, u);
         if (cur_chunk < 0) pdl_wait_previous();  // activations may come from the previous kernel
         if (chunk != cur_chunk) {
+            if constexpr (HasInputGate<P>::value) {
+                if (!__all_sync(0xffffffffu, P::wait_inputs(p, S.wait))) return;
+            }
             // Everyone is done with the previous columns before they change,
             // and the new ones are complete before anyone reads them. The
             // barriers are mbarriers so a wait can give up instead of hang.
@@ -1090,10 +1102,16 @@ __device__ void consumer_parts(const typename P::Params& p, const Smem& S, const
 //   __device__ static void stage(const Params&, int chunk, int kblk0, int kblk1, const StageDst&,
 //                                int tid, int nthreads);
 //   __device__ static void epilogue(const Params&, int u, const Sums<NT>&, int lane);
+//   optional: static constexpr bool kInputGate = true; and
+//   __device__ static bool wait_inputs(const Params&, const WaitCtx&) -- called by
+//   every consumer warp before it stages a chunk's activations (a problem whose
+//   activations another CTA of the same grid produces waits for them there;
+//   false = the wait gave up).
+// stream_body is the whole CTA program; a kernel may run it more than once
+// (one problem after another) on the same shared memory.
 template <class P, bool kParts>
-__global__ void __launch_bounds__(Roles<P>::kThreads, 1)
-    stream_kernel(const __grid_constant__ CUtensorMap tmap, const typename P::Params p) {
-    extern __shared__ uint8_t smem_raw[];
+__device__ __forceinline__ void stream_body(const CUtensorMap& tmap, const typename P::Params& p,
+                                            uint8_t* smem_raw) {
     const uint32_t raw = smem_addr(smem_raw);
     Smem S;
     S.base = (raw + 1023u) & ~1023u;
@@ -1206,6 +1224,37 @@ __global__ void __launch_bounds__(Roles<P>::kThreads, 1)
         // No CTA of a cluster leaves while another may still write to it.
         if (pl.cl > 1) cluster_sync_all();
     }
+}
+
+// Between two stream_body runs on the same shared memory, after every
+// thread of the CTA has left the first one and passed a __syncthreads:
+// returns whether that run gave up (its abort flag), and warp 0 invalidates
+// the mbarriers it initialised. The caller synchronises the CTA again before
+// the next run initialises its own.
+__device__ __forceinline__ bool stream_smem_release(const SmemLayout& L, uint8_t* smem_raw, bool parts) {
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const Bars bars{base + L.bars, L.nslot, L.nss, L.nrb, base + L.tags};
+    const bool aborted = *reinterpret_cast<volatile int*>(smem_raw + (bars.abort_flag() - raw)) != 0;
+    if (threadIdx.x < 32) {
+        for (uint32_t s = threadIdx.x; s < L.nslot; s += 32) {
+            mbar_inval(bars.full(s));
+            mbar_inval(bars.empty(s));
+        }
+        for (uint32_t s = threadIdx.x; s < L.nss; s += 32) {
+            mbar_inval(bars.sfull(s));
+            mbar_inval(bars.sempty(s));
+        }
+        if (threadIdx.x < (parts ? 4u : 3u)) mbar_inval(bars.xbar(threadIdx.x));
+    }
+    return aborted;
+}
+
+template <class P, bool kParts>
+__global__ void __launch_bounds__(Roles<P>::kThreads, 1)
+    stream_kernel(const __grid_constant__ CUtensorMap tmap, const typename P::Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    stream_body<P, kParts>(tmap, p, smem_raw);
 }
 
 // Host launcher: one CTA per SM (or clusters of p.cl CTAs), never more

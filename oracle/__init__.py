@@ -210,6 +210,15 @@ def moe(x, logits, top_k, w1, w2, inter, tok=None, cols=None, n_shared=0):
     return default().moe(x, logits, top_k, w1, w2, inter, tok, cols, n_shared)
 
 
+def ffn(x, w1q, w1s, w2q, w2s, inter, cols=None):
+    """Dense SwiGLU FFN y = W2 (SiLU(W1_gate x) * (W1_up x)) in float64: the
+    one-expert, top-1 MoE above (the softmax of a single logit is exactly 1,
+    so its gate weight multiplies by 1). Returns (y, rss) [t, ncols]."""
+    t = x.shape[0]
+    lg = np.zeros((t, 1), np.float32)
+    return default().moe(x, lg, 1, {0: (w1q, w1s)}, {0: (w2q, w2s)}, inter, cols=cols)
+
+
 def within_tolerance(y_gpu: np.ndarray, y_ref: np.ndarray, rss: np.ndarray,
                      rel: float = 4e-3, abs_rss: float = 1e-3) -> np.ndarray:
     """Elementwise |y - y_ref| <= rel*|y_ref| + abs_rss*rss (the stated bound)."""

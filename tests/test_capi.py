@@ -109,3 +109,27 @@ def test_moe_shared_argument_errors_return_before_launch(L):
         mx.mxfp4_moe_workspace_size(t, e, top_k, hidden, inter)
     assert call(a16=need - 1) == mx.MXFP4_ERR_WORKSPACE
     assert mx.mxfp4_moe_shared_workspace_size(t, e, top_k, -1, hidden, inter) == 0
+
+
+def test_ffn_argument_errors_return_before_launch(L):
+    import mxfp4_weight_streaming_gb300 as mx
+    p = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+    odd = ctypes.c_void_p(0x1001)
+    base = [p, 4, 256, p, p, p, p, 128, p, p, 1 << 30, None]
+
+    def call(**change):
+        a = list(base)
+        for i, v in change.items():
+            a[int(i[1:])] = v
+        return mx.mxfp4_ffn(*a)
+
+    assert call(a0=None) == mx.MXFP4_ERR_INVALID_ARG
+    assert call(a1=0) == mx.MXFP4_ERR_INVALID_ARG
+    assert call(a1=9) == mx.MXFP4_ERR_SHAPE  # t > 8
+    assert call(a2=48) == mx.MXFP4_ERR_SHAPE  # hidden % 32
+    assert call(a7=80) == mx.MXFP4_ERR_SHAPE  # inter % 32
+    assert call(a0=odd) == mx.MXFP4_ERR_ALIGN
+    assert call(a9=None) == mx.MXFP4_ERR_WORKSPACE
+    need = mx.mxfp4_ffn_workspace_size(4, 256, 128)
+    assert need >= 256 + 4 * 128 * 4
+    assert call(a10=need - 1) == mx.MXFP4_ERR_WORKSPACE

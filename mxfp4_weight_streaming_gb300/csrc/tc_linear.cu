@@ -75,21 +75,23 @@ constexpr int kFirstConverterWarp = 6;
 constexpr int kTmemCols = 512;
 
 // Shared-memory plan of one configuration (offsets from the 1024-aligned
-// base). A buffer i: SA atoms of 128 rows x 128 B. B buffer
-// j: NPAD rows x 128 B per atom (SA atoms), then the stage's activation
-// scale bytes, 16 per row (atom c's four block scales at bytes 4c..4c+3).
-// NG converter groups of W warps, one B buffer per group.
+// base). A buffer i: SA atoms of 128 rows x 128 B. B buffer j: NPAD rows x
+// 128 B per atom (SA atoms). Then the B buffers' activation scale images,
+// NPAD x 16 bytes each (row n's atom c block scales at bytes 16n + 4c ..
+// 16n + 4c + 3), packed after the B buffers so that no buffer pads to 1 KB
+// for them. NG converter groups of W warps, one B buffer per group.
 template <int NPAD, int SA, int NA, int NG, int W>
 struct Cfg {
     static constexpr int kConverters = NG * W;
     static constexpr int kThreads = (kFirstConverterWarp + kConverters) * 32;
     static constexpr int kAtomBytesB = NPAD * 128;
     static constexpr int kSlotA = SA * kAtomBytesA;
-    static constexpr int kSfbOff = SA * kAtomBytesB;
-    static constexpr int kSlotB = (kSfbOff + NPAD * 16 + 1023) / 1024 * 1024;
+    static constexpr int kSlotB = SA * kAtomBytesB;  // a multiple of 1024 (NPAD >= 16)
+    static constexpr int kImgBytes = NPAD * 16;
     static constexpr int kOffA = 0;
     static constexpr int kOffB = NA * kSlotA;
-    static constexpr int kOffBars = kOffB + NG * kSlotB;
+    static constexpr int kOffImg = kOffB + NG * kSlotB;
+    static constexpr int kOffBars = kOffImg + NG * kImgBytes;
     // mbarriers: fullA, emptyA, sfaReady [NA]; fullB, emptyB, sfbReady [NG];
     // accFull, accEmpty, inbox, drain; then the abort flag and the TMEM base
     // word.
@@ -105,8 +107,9 @@ struct Cfg {
     static constexpr int kMaxBatch = kSfaCol / NPAD;
     static_assert(NPAD % 16 == 0 && NPAD >= 16 && NPAD <= 64, "MMA N");
     static_assert(SA == 2 || SA == 4, "stage atoms");
-    // Byte of (B row n, stage atom c, 32-block kb) in the activation scales.
+    // Byte of (B row n, stage atom c, 32-block kb) in a scale image.
     __device__ static uint32_t sfb_byte(int n, int c, int kb) { return static_cast<uint32_t>(n * 16 + 4 * c + kb); }
+    static_assert(kSlotB % 1024 == 0, "B buffers stay 1024-aligned for the 128-byte swizzle");
     static constexpr int smem_bytes(int cl, int t) { return kOffInbox + (cl - 1) * t * kTileRows * 4; }
 };
 
@@ -339,7 +342,7 @@ __device__ __forceinline__ void load_blocks(const TcLinearParams& p, int atom0, 
 
 template <class C, int SA, int G>
 __device__ __forceinline__ void convert_blocks(const TcLinearParams& p, int b0, int lane, const XBlocks<G>& xb,
-                                               uint32_t b_smem) {
+                                               uint32_t b_smem, uint32_t img) {
     constexpr int kBlocksPerToken = 4 * SA;
     const int nblocks = p.T * kBlocksPerToken;
 #pragma unroll
@@ -356,7 +359,6 @@ __device__ __forceinline__ void convert_blocks(const TcLinearParams& p, int b0, 
         sts128(swz(atom, rh, 2 * kb + 1), hi[4], hi[5], hi[6], hi[7]);
         sts128(swz(atom, rl, 2 * kb), lo[0], lo[1], lo[2], lo[3]);
         sts128(swz(atom, rl, 2 * kb + 1), lo[4], lo[5], lo[6], lo[7]);
-        const uint32_t img = b_smem + C::kSfbOff;
         const uint32_t a_h = img + C::sfb_byte(rh, c, kb);
         const uint32_t a_l = img + C::sfb_byte(rl, c, kb);
         asm volatile("st.shared.u8 [%0], %1;" ::"r"(a_h), "r"(sbyte) : "memory");
@@ -375,6 +377,7 @@ __device__ void converter(const TcLinearParams& p, int cw, int lane, const Work&
     const int g = cw / W, m = cw % W;
     const int nchunks = w.nbatch * w.spt;
     const uint32_t b_smem = base + C::kOffB + g * C::kSlotB;
+    const uint32_t img = base + C::kOffImg + g * C::kImgBytes;
     const int nblocks = p.T * 4 * SA;
     for (int i = g, r = 0; i < nchunks; i += NG, ++r) {
         const int atom0 = (w.st0 + i % w.spt) * SA;
@@ -382,10 +385,10 @@ __device__ void converter(const TcLinearParams& p, int cw, int lane, const Work&
         XBlocks<G> xb;
         load_blocks<SA, G>(p, atom0, 32 * m * G, lane, xb);
         if (!__all_sync(0xffffffffu, mbar_wait(bars.empty_b(g), (static_cast<uint32_t>(r) & 1u) ^ 1u, wc))) return;
-        convert_blocks<C, SA, G>(p, 32 * m * G, lane, xb, b_smem);
+        convert_blocks<C, SA, G>(p, 32 * m * G, lane, xb, b_smem, img);
         for (int b0 = 32 * G * (m + W); b0 < nblocks; b0 += 32 * G * W) {
             load_blocks<SA, G>(p, atom0, b0, lane, xb);
-            convert_blocks<C, SA, G>(p, b0, lane, xb, b_smem);
+            convert_blocks<C, SA, G>(p, b0, lane, xb, b_smem, img);
         }
         fence_proxy_async_shared();  // generic-proxy writes -> visible to the tensor core's reads
         __syncwarp();
@@ -466,7 +469,7 @@ __device__ void epilogue(const TcLinearParams& p, int q, int lane, const Work& w
                     if (!weight_scales(ti)) return;
             if (!__all_sync(0xffffffffu, mbar_wait(bars.full_b(rb.slot), rb.phase, wc))) return;
             {
-                const uint32_t img = base + C::kOffB + rb.slot * C::kSlotB + C::kSfbOff;
+                const uint32_t img = base + C::kOffImg + rb.slot * C::kImgBytes;
                 const uint4 v0 = lds128(img + lane * 16);
                 const uint4 v1 = NPAD > 32 ? lds128(img + (lane + 32) * 16) : make_uint4(0u, 0u, 0u, 0u);
                 store_b_scale_words(tbase + lanes + C::kSfbCol + rb.slot * 16, v0, v1);
@@ -577,7 +580,7 @@ __global__ void __launch_bounds__(Cfg<NPAD, SA, NA, NG, W>::kThreads, 1)
     }
     // B buffers start at zero: padding rows (tokens beyond T) and unused
     // scale-image bytes stay zero for the whole kernel.
-    for (int i = threadIdx.x; i < NG * C::kSlotB / 16; i += C::kThreads)
+    for (int i = threadIdx.x; i < (C::kOffBars - C::kOffB) / 16; i += C::kThreads)  // buffers and images
         sts128(base + C::kOffB + 16 * i, 0u, 0u, 0u, 0u);
     fence_proxy_async_shared();
     fence_before_sync();
@@ -651,10 +654,17 @@ struct Launcher {
     }
 };
 
-// Configurations by token count: (NPAD, SA, NA, NG, W).
-using CfgT8 = Launcher<16, 4, 3, 3, 1>;
-using CfgT16 = Launcher<32, 2, 5, 3, 1>;
-using CfgT32 = Launcher<64, 2, 4, 3, 2>;
+// Configurations (NPAD, SA, NA, NG, W) by token count. Lone CTAs take
+// 4-atom stages wherever the activation buffers leave room for three of them
+// (a copy of 4 atoms costs the copy engine about as long as one of 2, so
+// stages of 4 halve that cost per byte); T > 16 fits only 2-atom stages. A
+// cluster of 2 that splits K needs T x 128 x 4 more bytes for its inbox,
+// so the split configurations keep smaller rings.
+using CfgT8 = Launcher<16, 4, 3, 3, 1>;        // lone and split
+using CfgT16 = Launcher<32, 4, 3, 2, 2>;       // lone
+using CfgT16Split = Launcher<32, 2, 5, 3, 1>;  // split
+using CfgT32 = Launcher<64, 2, 5, 3, 2>;       // lone
+using CfgT32Split = Launcher<64, 2, 4, 3, 2>;  // split
 
 // Token counts below this go to the streaming engine, which measured faster
 // there on GB300: its weight ring holds packed codes (one smem byte per HBM
@@ -664,44 +674,82 @@ using CfgT32 = Launcher<64, 2, 4, 3, 2>;
 // tensor-core kernel is faster (at t = 16 and 32 by 1.3x and 2.3x).
 constexpr int kMinTokens = 5;
 
-int atoms_per_stage(int t) { return t <= 8 ? CfgT8::kSA : (t <= 16 ? CfgT16::kSA : CfgT32::kSA); }
+enum CfgId { kT8, kT16, kT16Split, kT32, kT32Split };
 
-static int smem_for(int t, int cl) {
-    return t <= 8 ? CfgT8::smem(cl, t) : (t <= 16 ? CfgT16::smem(cl, t) : CfgT32::smem(cl, t));
+static CfgId cfg_id(int t, int cl) {
+    if (t <= 8) return kT8;
+    if (t <= 16) return cl > 1 ? kT16Split : kT16;
+    return cl > 1 ? kT32Split : kT32;
 }
 
-static int ring_slots(int t) { return t <= 8 ? CfgT8::kNA : (t <= 16 ? CfgT16::kNA : CfgT32::kNA); }
+static int cfg_atoms(CfgId id) {
+    switch (id) {
+        case kT8: return CfgT8::kSA;
+        case kT16: return CfgT16::kSA;
+        case kT16Split: return CfgT16Split::kSA;
+        case kT32: return CfgT32::kSA;
+        default: return CfgT32Split::kSA;
+    }
+}
+
+static int cfg_slots(CfgId id) {
+    switch (id) {
+        case kT8: return CfgT8::kNA;
+        case kT16: return CfgT16::kNA;
+        case kT16Split: return CfgT16Split::kNA;
+        case kT32: return CfgT32::kNA;
+        default: return CfgT32Split::kNA;
+    }
+}
+
+static int cfg_smem(CfgId id, int cl, int t) {
+    switch (id) {
+        case kT8: return CfgT8::smem(cl, t);
+        case kT16: return CfgT16::smem(cl, t);
+        case kT16Split: return CfgT16Split::smem(cl, t);
+        case kT32: return CfgT32::smem(cl, t);
+        default: return CfgT32Split::smem(cl, t);
+    }
+}
+
+int atoms_per_stage(int t, int cl) { return cfg_atoms(cfg_id(t, cl)); }
 
 bool plan_tc(int t, int64_t k, int64_t n, int num_sms, int max_smem, TcPlan* out) {
     // k % 512: every stage lies inside one 4-atom scale group, whose 16
     // bytes per row are one aligned vector load.
     if (t < kMinTokens || t > 32 || k % 512 != 0 || n < 1) return false;
-    const int sa = atoms_per_stage(t);
-    const int64_t stages = k / 128 / sa;
     const int64_t tiles = (n + kTileRows - 1) / kTileRows;
-    if (stages >= (int64_t(1) << 30) || tiles >= (int64_t(1) << 30)) return false;
+    if (k / 128 >= (int64_t(1) << 30) || tiles >= (int64_t(1) << 30)) return false;
     // A cluster of 2 splits K when one tile per CTA would leave half the
     // SMs idle (one tile per cluster; every CTA keeps >= 1 stage).
     int cl = 1;
-    if (2 * tiles <= num_sms && stages >= 2 && smem_for(t, 2) <= max_smem) cl = 2;
-    if (smem_for(t, cl) > max_smem) return false;
+    if (2 * tiles <= num_sms) {
+        const CfgId s2 = cfg_id(t, 2);
+        if (k / 128 / cfg_atoms(s2) >= 2 && cfg_smem(s2, 2, t) <= max_smem) cl = 2;
+    }
+    const CfgId id = cfg_id(t, cl);
+    if (cfg_smem(id, cl, t) > max_smem) return false;
     TcPlan r{};
     r.cl = cl;
     r.grid = cl > 1 ? static_cast<int>(cl * tiles) : static_cast<int>(tiles < num_sms ? tiles : num_sms);
-    r.atoms_per_stage = sa;
-    r.stages = static_cast<int>(stages);
+    r.atoms_per_stage = cfg_atoms(id);
+    r.stages = static_cast<int>(k / 128 / r.atoms_per_stage);
     r.tiles = static_cast<int>(tiles);
-    r.ring_slots = ring_slots(t);
-    r.smem_bytes = smem_for(t, cl);
+    r.ring_slots = cfg_slots(id);
+    r.smem_bytes = cfg_smem(id, cl, t);
     *out = r;
     return true;
 }
 
 cudaError_t launch_tc_linear(const CUtensorMap& amap, const TcLinearParams& p, const TcPlan& plan,
                              cudaStream_t stream) {
-    if (p.T <= 8) return CfgT8::launch(amap, p, plan.grid, stream);
-    if (p.T <= 16) return CfgT16::launch(amap, p, plan.grid, stream);
-    return CfgT32::launch(amap, p, plan.grid, stream);
+    switch (cfg_id(p.T, plan.cl)) {
+        case kT8: return CfgT8::launch(amap, p, plan.grid, stream);
+        case kT16: return CfgT16::launch(amap, p, plan.grid, stream);
+        case kT16Split: return CfgT16Split::launch(amap, p, plan.grid, stream);
+        case kT32: return CfgT32::launch(amap, p, plan.grid, stream);
+        default: return CfgT32Split::launch(amap, p, plan.grid, stream);
+    }
 }
 
 }  // namespace tc

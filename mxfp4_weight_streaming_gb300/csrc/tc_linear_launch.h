@@ -37,8 +37,9 @@ struct TcPlan {
 // scale bytes 16-byte aligned (one vector load per row).
 bool plan_tc(int t, int64_t k, int64_t n, int num_sms, int max_smem, TcPlan* out);
 
-// atoms_per_stage(t): the stage size plan_tc picks (the tensor map's box depth).
-int atoms_per_stage(int t);
+// atoms_per_stage(t, cl): the stage size plan_tc picks for t tokens and
+// cluster size cl (the tensor map's box depth).
+int atoms_per_stage(int t, int cl);
 
 // amap: the packed codes (16U4_ALIGN16B, 3D, box 128 values x 128 rows x
 // atoms_per_stage).

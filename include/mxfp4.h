@@ -19,7 +19,9 @@
  *
  * Conventions for every call:
  *   - All pointers are device memory owned by the caller. The library
- *     allocates nothing; the MoE scratch comes from the caller's workspace.
+ *     allocates nothing; the MoE and FFN scratch comes from the caller's
+ *     workspace. Exception: mxfp4_moe_noalloc keeps its scratch in one
+ *     fixed array of the library (see there).
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Calls
  *     only enqueue work and return; results are ready when the stream is.
  *   - Argument errors are returned before anything is launched. A failed
@@ -29,7 +31,13 @@
  *     mxfp4_last_device_status() reports (and clears) that word.
  *   - Identical inputs give bit-identical outputs (no floating-point
  *     atomics); calls are stateless and thread-safe apart from the
- *     caller's own buffers.
+ *     caller's own buffers. Exception: calls of mxfp4_moe_noalloc that
+ *     overlap on the GPU (unordered streams, or threads) race on its
+ *     shared scratch array.
+ *   - The first call on a device looks up per-device addresses (the status
+ *     word, the mxfp4_moe_noalloc scratch) and keeps them for the life of
+ *     the process. After cudaDeviceReset, or anything else that replaces
+ *     the device's primary context, unload and reload the library.
  *   - There is no CPU path: without a GB300-class GPU every compute call
  *     returns MXFP4_ERR_CUDA.
  */
@@ -90,10 +98,23 @@ int mxfp4_quantize(const float* w, int64_t n, int64_t k, uint8_t* wq, uint8_t* w
  *   n   output features (>= 1, < 2^31)
  *   y   device bf16 [t, n], row-major, 2-byte aligned (output)
  * Accumulation is fp32 (tensor-core fp32 accumulate); the summation order
- * is the kernel's. Returns MXFP4_ERR_SHAPE when no shared-memory plan fits
- * (mxfp4_linear_plan reports the plan). The binding limit is k: a row
- * group's scale bytes for all of k (k/2 bytes) stay on chip next to the
- * staging buffers. Every t <= 32 and n plans for k <= 262144 on GB300.
+ * is the kernel's. Two kernels serve the call (mxfp4_linear_plan says which):
+ *   - t <= 4, or k % 512 != 0, or wq not 32-byte aligned: the streaming
+ *     engine (E2M1 -> f16 in registers, mma.sync, fp32 block scaling).
+ *   - otherwise (5 <= t <= 32): the block-scaled tensor-core kernel
+ *     (tcgen05.mma kind::mxf8f6f4: the E2M1 codes and E8M0 scales go to
+ *     the tensor cores as stored). Its other operand is 8-bit, so each bf16
+ *     activation is split into two E4M3 pieces under one power-of-two scale
+ *     per (token, 32 values) -- the pages' production format pairs MXFP4
+ *     weights with MXFP8 activations ("Zyphra Inference Wave 2", section
+ *     "Quantization"; AMD "megakernel-intro", section "3. Low-Precision
+ *     Data Types"). The split is exact for values within 2^9 of their
+ *     block's largest magnitude; smaller ones keep an absolute error below
+ *     2^-17 of that maximum, far inside the tolerance's RSS term.
+ * Returns MXFP4_ERR_SHAPE when no shared-memory plan fits. The binding
+ * limit is k: a row group's scale bytes for all of k (k/2 bytes) stay on
+ * chip next to the staging buffers. Every t <= 32 and n plans for
+ * k <= 262144 on GB300.
  */
 int mxfp4_linear(const void* x, int64_t t, int64_t k, const uint8_t* wq, const uint8_t* ws, int64_t n,
                  void* y, void* stream);
@@ -110,19 +131,24 @@ int mxfp4_linear(const void* x, int64_t t, int64_t k, const uint8_t* wq, const u
  *              (cudaDevAttrMaxSharedMemoryPerBlockOptin)
  *   out        host struct, written on MXFP4_OK (caller-owned)
  * Host only: no CUDA call, no device needed. Returns MXFP4_ERR_SHAPE when
- * mxfp4_linear would (no plan fits max_smem).
+ * mxfp4_linear would (no plan fits max_smem). It takes wq to be 32-byte
+ * aligned (a mode-3 shape whose wq is not runs the streaming engine).
  */
 typedef struct {
     int32_t mode;        /* 0: whole K per CTA; 1: K walked in parts per CTA;
-                            2: K split over a thread-block cluster */
+                            2: K split over a thread-block cluster (modes 0-2:
+                            the streaming engine); 3: the block-scaled
+                            tensor-core kernel (cluster 2 = K split) */
     int32_t ctas;        /* CTAs launched (mode 2: an upper bound; the number
                             of co-resident clusters decides) */
     int32_t cluster;     /* CTAs per cluster (1 unless mode 2) */
     int32_t stage_steps; /* K steps of 256 values per weight-ring stage */
-    int32_t chunk_steps; /* K steps a consumer warp takes at a time */
+    int32_t chunk_steps; /* K steps a consumer warp takes at a time (mode 3:
+                            a whole stage) */
     int32_t ring_slots;  /* stages in the weight ring */
     int32_t part_steps;  /* mode 1: K steps per part; else 0 */
-    int32_t batch_units; /* mode 1: row groups of 16 rows per batch; else 0 */
+    int32_t batch_units; /* mode 1: row groups of 16 rows per batch; mode 3:
+                            128-row tiles per CTA at most; else 0 */
     int32_t smem_bytes;  /* dynamic shared memory per CTA */
 } mxfp4_linear_plan_t;
 int mxfp4_linear_plan(int64_t t, int64_t k, int64_t n, int num_sms, int max_smem, mxfp4_linear_plan_t* out);

@@ -20,8 +20,8 @@ per-call time). Clocks are sampled with nvidia-smi while each workload runs.
 
 Besides the headline line's `value`, the default run times every other
 configuration of the method (the T=1 K=N=1024 linear, the LM head, the FFN
-token sweep and the grouped MoE) under a `workloads` key, each with its own
-clock summary.
+token sweep, the fused FFN chain and the grouped MoE at T=32 and T=128)
+under a `workloads` key, each with its own clock summary.
 """
 from __future__ import annotations
 
@@ -59,6 +59,12 @@ WORKLOADS = {
 DEFAULT_WORKLOAD = "verify_t4_k7168_n7168"
 MOE_WORKLOAD = "moe_e256_top8_t32"
 MOE = dict(t=32, e=256, top_k=8, hidden=7168, inter=2048, seed=4)
+# The grouped MoE at a larger token count (every expert receives several
+# chunks of tokens), timed beside the T=32 configuration.
+MOE_LARGE_T = 128
+# Fused dense FFN chain (mxfp4_ffn): W1 [2*inter, hidden] then W2 [hidden,
+# inter], hidden 7168 and inter 9216 (the FFN width of the up projection).
+FFN_CHAIN = {f"ffn_chain_t{t}_h7168_i9216": dict(t=t, hidden=7168, inter=9216, seed=3) for t in (1, 2, 4)}
 
 
 def algorithmic_bytes(t: int, k: int, n: int) -> int:
@@ -446,16 +452,66 @@ def moe_expert_bytes(hidden: int, inter: int) -> int:
     return 2 * inter * (hidden // 2 + hidden // 32) + hidden * (inter // 2 + inter // 32)
 
 
-def run_moe(steps: int, device, clocks, replays: int = 10):
-    """Grouped top-8 MoE decode step (256 experts, T=32): one mxfp4_moe call
-    per step; bytes = distinct routed experts' W1+W2 (+ x, logits, y)."""
+def ffn_chain_bytes(t: int, hidden: int, inter: int) -> int:
+    return int(0.53125 * 3 * inter * hidden) + 2 * t * hidden + 2 * t * hidden
+
+
+def measure_ffn_chain(wl_name: str, device, clocks, calls_target: int = 1200, replays: int = 12):
+    """Fused dense FFN chain (one mxfp4_ffn call = one cooperative launch
+    plus a 4-byte memset): per-call time and GB/s of W1 + W2 (+ x, y)."""
     import torch
 
     import mxfp4_weight_streaming_gb300 as mx
     import synth
 
-    m = MOE
-    t, e, top_k, hidden, inter, seed = m["t"], m["e"], m["top_k"], m["hidden"], m["inter"], m["seed"]
+    wl = FFN_CHAIN[wl_name]
+    t, hidden, inter, seed = wl["t"], wl["hidden"], wl["inter"], wl["seed"]
+    w1q, w1s = mx.quantize(synth.weights(seed, 2 * inter, hidden, device=device))
+    w2q, w2s = mx.quantize(synth.weights(seed, hidden, inter, tid=synth.TID_W2, device=device))
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    wbytes = w1q.numel() + w1s.numel() + w2q.numel() + w2s.numel()
+    copies = max(1, math.ceil(2 * l2 / wbytes) + 1) if wbytes < 2 * l2 else 1
+    sets = [(w1q, w1s, w2q, w2s)] + [tuple(a.clone() for a in (w1q, w1s, w2q, w2s)) for _ in range(copies - 1)]
+    ptrs = [tuple(a.data_ptr() for a in st) for st in sets]
+    x = synth.tokens(seed, t, hidden, device=device)
+    y = torch.empty((t, hidden), dtype=torch.bfloat16, device=device)
+    ws = torch.empty(mx.mxfp4_ffn_workspace_size(t, hidden, inter), dtype=torch.uint8, device=device)
+    stream = torch.cuda.Stream(device)
+    lib = mx.load()
+
+    def call(i):
+        p = ptrs[i % copies]
+        rc = lib.mxfp4_ffn(x.data_ptr(), t, hidden, p[0], p[1], p[2], p[3], inter, y.data_ptr(), ws.data_ptr(),
+                           ws.numel(), stream.cuda_stream)
+        if rc != 0:
+            raise RuntimeError(mx.strerror(rc))
+
+    G = max(copies, min(128, calls_target // replays) // copies * copies)
+    timer = GraphTimer(call, G, stream)
+    timer.soak(0.4)
+    wall0 = time.time()
+    ms, per_call = timer.run(replays)
+    wall1 = time.time()
+    calls = replays * G
+    us = ms * 1e3 / calls
+    nbytes = ffn_chain_bytes(t, hidden, inter)
+    peak, _ = hbm_peak()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"us_per_call": round(us, 3), "GBps": round(gbs, 1), "frac": round(gbs / peak, 4),
+            "spread_us_per_call": percentiles(per_call), "calls": calls, "bytes_per_call": nbytes,
+            "kernel": "mxfp4::ffn_chain_kernel (stream_body<FfnUp> then stream_body<FfnDown>, cooperative)",
+            "launches_per_call": 1, "memsets_per_call": 1,
+            "clocks": clocks.summary(wall0 - 0.5, wall1 + 0.1)}
+
+
+_MOE_WEIGHTS = {}  # the expert weights, shared by the MoE runs of one bench process
+
+
+def moe_weights(device, e, hidden, inter, seed):
+    import torch
+
+    import mxfp4_weight_streaming_gb300 as mx
+    import synth
     w1q = torch.empty((e, 2 * inter, hidden // 2), dtype=torch.uint8, device=device)
     w1s = torch.empty((e, 2 * inter, hidden // 32), dtype=torch.uint8, device=device)
     w2q = torch.empty((e, hidden, inter // 2), dtype=torch.uint8, device=device)
@@ -470,6 +526,26 @@ def run_moe(steps: int, device, clocks, replays: int = 10):
         w2q[ex].copy_(q.view(hidden, -1))
         w2s[ex].copy_(sc.view(hidden, -1))
         del a, b
+    return w1q, w1s, w2q, w2s
+
+
+def run_moe(steps: int, device, clocks, replays: int = 10, t: int | None = None):
+    """Grouped top-8 MoE decode step (256 experts, T=32 unless t is given):
+    one mxfp4_moe call per step; bytes = distinct routed experts' W1+W2 (+ x,
+    logits, y)."""
+    import torch
+
+    import mxfp4_weight_streaming_gb300 as mx
+    import synth
+
+    m = MOE
+    e, top_k, hidden, inter, seed = m["e"], m["top_k"], m["hidden"], m["inter"], m["seed"]
+    t = m["t"] if t is None else t
+    key = (str(device), e, hidden, inter, seed)
+    if key not in _MOE_WEIGHTS:
+        _MOE_WEIGHTS.clear()
+        _MOE_WEIGHTS[key] = moe_weights(device, e, hidden, inter, seed)
+    w1q, w1s, w2q, w2s = _MOE_WEIGHTS[key]
     x = synth.tokens(seed, t, hidden, device=device)
     lg = synth.logits(seed, t, e, device=device)
     distinct = int(torch.unique(torch.topk(lg.cpu(), top_k, dim=1).indices).numel())
@@ -626,10 +702,22 @@ def main():
             torch.cuda.empty_cache()
         cache.clear()
         torch.cuda.empty_cache()
+        for name in FFN_CHAIN:
+            try:
+                extra[name] = measure_ffn_chain(name, device, clocks)
+            except Exception as ex:
+                extra[name] = {"error": str(ex)[:300]}
+            torch.cuda.empty_cache()
         try:
             extra[MOE_WORKLOAD] = run_moe(200, device, clocks)
         except Exception as ex:
             extra[MOE_WORKLOAD] = {"error": str(ex)[:300]}
+        torch.cuda.empty_cache()
+        try:
+            extra[f"moe_e256_top8_t{MOE_LARGE_T}"] = run_moe(100, device, clocks, t=MOE_LARGE_T)
+        except Exception as ex:
+            extra[f"moe_e256_top8_t{MOE_LARGE_T}"] = {"error": str(ex)[:300]}
+        _MOE_WEIGHTS.clear()
         torch.cuda.empty_cache()
         res["workloads"] = extra
     clocks.stop()

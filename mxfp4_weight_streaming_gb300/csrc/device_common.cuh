@@ -125,17 +125,17 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p) {
 }
 
 // Waits until the device word at p is at least want (counted by other CTAs
-// of the grid, which must all be resident). Same limits as mbar_wait.
+// of the grid, which must all be resident). Same limits as mbar_wait. No
+// sleep between reads: each acquire load is already an L2 round trip, and
+// a sleep measured as 1-2 us of lag between the last count and the waiters.
 __device__ __forceinline__ bool wait_global_at_least(const unsigned* p, unsigned want, const WaitCtx& w) {
     if (ld_acquire_gpu(p) >= want) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
         if (*w.abort) return false;
 #pragma unroll 1
-        for (int i = 0; i < 32; ++i) {
-            __nanosleep(64);
+        for (int i = 0; i < 32; ++i)
             if (ld_acquire_gpu(p) >= want) return true;
-        }
         if (global_timer_ns() - t0 > kWaitLimitNs) {
             record_timeout(w);
             return false;

@@ -15,7 +15,7 @@
 // the same shared memory:
 //   phase A: units of 16 gate + 16 up rows over K = hidden, x staged once;
 //            the epilogue stores h and counts the unit in a device word.
-//   phase B: units of 32 W2 rows over K = inter. The producer starts
+//   phase B: units of 16 W2 rows over K = inter. The producer starts
 //            streaming W2 as soon as its CTA has finished phase A; the
 //            consumers wait (bounded) until every CTA's phase-A units are
 //            counted, then stage h as two f16 columns per token (hi + lo,
@@ -103,13 +103,16 @@ struct FfnDownParams {
 template <int NT_>
 struct FfnDownProblem {
     static constexpr int NT = NT_;
-    static constexpr int BOXES = 2;
+    // 16-row units: hidden / 16 of them spread evenly over the SMs (32-row
+    // units left a third of the CTAs with one unit less than the rest), and
+    // the smaller stages leave more ring slots beside the staged h.
+    static constexpr int BOXES = 1;
     static constexpr int NCW = 11;
     using Params = FfnDownParams;
 
-    __device__ static int num_units(const Params& p) { return p.hidden / 32; }
+    __device__ static int num_units(const Params& p) { return p.hidden / 16; }
     __device__ static int chunk_of(const Params&, int) { return 0; }
-    __device__ static int box_row(const Params&, int u, int box) { return 32 * u + 16 * box; }
+    __device__ static int box_row(const Params&, int u, int) { return 16 * u; }
     __device__ static const uint8_t* scale_src(const Params& p, int u, int box) {
         return p.w2s + (size_t)box_row(p, u, box) * p.nblk;
     }
@@ -157,14 +160,12 @@ struct FfnDownProblem {
     }
 
     __device__ static void epilogue(const Params& p, int u, const Sums<NT>& v, int lane) {
-#pragma unroll
-        for (int bx = 0; bx < 2; ++bx)
-            for (int e = lane; e < p.T * 16; e += 32) {
-                const int t = e >> 4;
-                const int r = e & 15;
-                const float s = v.sum(bx, t, r) + v.sum(bx, p.T + t, r);
-                p.y[(size_t)t * p.hidden + 32 * u + 16 * bx + r] = __float2bfloat16_rn(s);
-            }
+        for (int e = lane; e < p.T * 16; e += 32) {
+            const int t = e >> 4;
+            const int r = e & 15;
+            const float s = v.sum(0, t, r) + v.sum(0, p.T + t, r);
+            p.y[(size_t)t * p.hidden + 16 * u + r] = __float2bfloat16_rn(s);
+        }
     }
 };
 
@@ -235,12 +236,12 @@ int plan_ffn(int t, int hidden, int inter, int max_smem, FfnPlan* out) {
     // grouped MoE's measured choices for the same two problems).
     const int steps1 = stage_steps(2, nkb1, 0);
     const int group1 = steps1 % 2 == 0 ? steps1 / 2 : steps1;
-    const int steps2 = stage_steps(2, nkb2, 0);
+    const int steps2 = stage_steps(1, nkb2, 0);
     pl.nt2 = 2 * t <= 8 ? 1 : 2;
     if (!plan_layout(1, 2, nblk1, nblk1, t, 1, FfnUpProblem::NCW, kRedStride, steps1, group1, nkb1, max_smem,
                      &pl.up))
         return MXFP4_ERR_SHAPE;
-    if (!plan_layout(pl.nt2, 2, nblk2, nblk2, 2 * t, 1, FfnUpProblem::NCW, kRedStride, steps2, steps2, nkb2,
+    if (!plan_layout(pl.nt2, 1, nblk2, nblk2, 2 * t, 1, FfnUpProblem::NCW, kRedStride, steps2, steps2, nkb2,
                      max_smem, &pl.down))
         return MXFP4_ERR_SHAPE;
     const uint32_t total = pl.up.total > pl.down.total ? pl.up.total : pl.down.total;
@@ -294,7 +295,7 @@ int launch_ffn(const FfnArgs& a, int num_sms, int max_smem, cudaStream_t stream)
     if (int rc = encode_weights(&map2, a.w2q, a.hidden, a.inter, static_cast<int>(pl.down.steps), &down.tma3d))
         return rc;
 
-    const int units = a.inter / 16 > a.hidden / 32 ? a.inter / 16 : a.hidden / 32;
+    const int units = a.inter / 16 > a.hidden / 16 ? a.inter / 16 : a.hidden / 16;
     const int grid = units < num_sms ? units : num_sms;
     if (cudaMemsetAsync(done, 0, sizeof(unsigned), stream) != cudaSuccess) return MXFP4_ERR_CUDA;
     const cudaError_t e = pl.nt2 == 1 ? launch_chain<1>(map1, map2, up, down, pl.smem_bytes, grid, stream)

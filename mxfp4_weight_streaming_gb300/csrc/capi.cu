@@ -118,6 +118,58 @@ namespace mxfp4 {
 int encode_weights(CUtensorMap* map, const uint8_t* wq, int64_t rows, int64_t k, int steps, int* is3d) {
     return encode_weight_map(map, wq, rows, k, steps, is3d);
 }
+
+// One copy per stage for units whose boxes are consecutive 16-row groups:
+// the 3D view with a box of box_rows rows (mode 2 of the engine). Falls back
+// to encode_weights (mode 0) when k % 256 != 0.
+int encode_weights_merged_rows(CUtensorMap* map, const uint8_t* wq, int64_t rows, int64_t k, int steps, int box_rows,
+                               int* mode) {
+    if (k % 256 == 0) {
+        cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(k / 256)};
+        cuuint64_t strides[2] = {static_cast<cuuint64_t>(k / 2), 128};
+        cuuint32_t box[3] = {128, static_cast<cuuint32_t>(box_rows), static_cast<cuuint32_t>(steps)};
+        cuuint32_t estride[3] = {1, 1, 1};
+        const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(wq), dims, strides, box,
+                                    estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r == CUDA_SUCCESS) {
+            *mode = 2;
+            return MXFP4_OK;
+        }
+    }
+    int is3d = 0;
+    const int rc = encode_weight_map(map, wq, rows, k, steps, &is3d);
+    *mode = is3d;
+    return rc;
+}
+
+// One copy per stage for gate/up units of W1 [e][2*inter][k/2] (16 gate rows
+// and the 16 up rows inter rows below them): the 5D view (128 B, 16 rows,
+// gate/up, 16-row group, k/256) with strides (k/2, inter*k/2, 16*k/2, 128 B)
+// and a box of one group's gate and up rows (mode 3 of the engine). A unit
+// starting at row r (a gate row, r % 16 == 0) is group r / 16. Falls back to
+// encode_weights (mode 0) when k % 256 != 0.
+int encode_weights_gate_up(CUtensorMap* map, const uint8_t* w1q, int64_t experts, int64_t inter, int64_t k, int steps,
+                           int* mode) {
+    if (k % 256 == 0 && inter % 16 == 0) {
+        cuuint64_t dims[5] = {128, 16, 2, static_cast<cuuint64_t>(experts * inter / 8), static_cast<cuuint64_t>(k / 256)};
+        cuuint64_t strides[4] = {static_cast<cuuint64_t>(k / 2), static_cast<cuuint64_t>(inter * (k / 2)),
+                                 static_cast<cuuint64_t>(16 * (k / 2)), 128};
+        cuuint32_t box[5] = {128, 16, 2, 1, static_cast<cuuint32_t>(steps)};
+        cuuint32_t estride[5] = {1, 1, 1, 1, 1};
+        const CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<uint8_t*>(w1q), dims, strides,
+                                    box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r == CUDA_SUCCESS) {
+            *mode = 3;
+            return MXFP4_OK;
+        }
+    }
+    int is3d = 0;
+    const int rc = encode_weight_map(map, w1q, experts * 2 * inter, k, steps, &is3d);
+    *mode = is3d;
+    return rc;
+}
 }  // namespace mxfp4
 
 namespace {

@@ -59,6 +59,26 @@ struct Roles {
     static constexpr int kConsumerThreads = P::NCW * 32;
 };
 constexpr int kBoxBytes = 2048;  // 16 rows x 128 bytes = 16 rows x 256 K values
+
+// How the producer copies a stage (Params::tma3d):
+//   0: 2D map [rows, K/2 B], one 16-row x 128-byte box per step and box;
+//   1: 3D map (128 B, rows, K/256), one copy per box of 16 rows x spb steps;
+//   kCopyMerged3d: 3D map whose box is 16 * BOXES rows high, the boxes of a
+//      unit being consecutive rows: one copy per stage;
+//   kCopyMerged5d: 5D map (128 B, 16 rows, box, 16-row group, K/256) whose
+//      box-index stride is the distance between a unit's boxes (the gate and
+//      up rows of an expert): one copy per stage.
+// The merged copies land a stage as [step][box][16 rows][128 B].
+constexpr int kCopyMerged3d = 2;
+constexpr int kCopyMerged5d = 3;
+
+__device__ __forceinline__ void issue_merged_stage(int mode, uint32_t dst, const CUtensorMap* tmap, int row0, int kb,
+                                                   uint32_t bar, uint64_t policy) {
+    if (mode == kCopyMerged3d)
+        tma_load_3d(dst, tmap, 0, row0, kb, bar, policy);
+    else
+        tma_load_5d(dst, tmap, 0, 0, 0, row0 / 16, kb, bar, policy);
+}
 constexpr int kRedStride = 20;   // floats per column row of the reduction area (16 + 4 pad)
 
 // mbarriers and tag words of one CTA (shared addresses), in the order the
@@ -597,10 +617,13 @@ __device__ void producer_role(const typename P::Params& p, const Smem& S, const 
                 continue;
             }
             mbar_arrive_expect_tx(bars.full(slot), stage_bytes);
-            // Stage layout: [box][step][16 rows][128 B], 128-byte swizzle.
             const uint32_t sbase = S.base + L.ring + slot * stage_bytes;
-            if (p.tma3d) {
-                // One copy per box: 16 rows x spb 128-byte segments of K.
+            if (p.tma3d >= kCopyMerged3d) {
+                // One copy for every box of the stage: [step][box][16 rows][128 B].
+                issue_merged_stage(p.tma3d, sbase, tmap, rows[0], pl.kb0 + st, bars.full(slot), policy);
+            } else if (p.tma3d) {
+                // Stage layout [box][step][16 rows][128 B], 128-byte swizzle: one
+                // copy per box of 16 rows x spb 128-byte segments of K.
 #pragma unroll
                 for (int bx = 0; bx < BOXES; ++bx)
                     tma_load_3d(sbase + bx * spb * kBoxBytes, tmap, 0, rows[bx], pl.kb0 + st, bars.full(slot),
@@ -693,10 +716,11 @@ __device__ void producer_parts(const typename P::Params& p, const Smem& S, const
             // slot's full barrier without mistaking an older phase for it.
             sts_u32_volatile(bars.ring_tag(slot), staged);
             mbar_arrive_expect_tx(bars.full(slot), stage_bytes);
-            // Stage layout: [box][step][16 rows][128 B], 128-byte swizzle.
             const uint32_t sbase = S.base + L.ring + slot * stage_bytes;
-            if (p.tma3d) {
-                // One copy per box: 16 rows x spb 128-byte segments of K.
+            if (p.tma3d >= kCopyMerged3d) {
+                issue_merged_stage(p.tma3d, sbase, tmap, rows[0], kb, bars.full(slot), policy);
+            } else if (p.tma3d) {
+                // Stage layout [box][step][16 rows][128 B]: one copy per box.
 #pragma unroll
                 for (int bx = 0; bx < BOXES; ++bx)
                     tma_load_3d(sbase + bx * spb * kBoxBytes, tmap, 0, rows[bx], kb, bars.full(slot), policy);
@@ -772,7 +796,10 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
     const uint32_t red0 = lone ? S.base + L.red : map_to_rank(S.base + L.red, 0);  // rank 0's buffers
     const uint32_t count0 = lone ? 0u : map_to_rank(bars.red_count(0), 0);
     const uint32_t ring = S.base + L.ring;
-    const uint32_t box_stride = spb * kBoxBytes;
+    // Stage layout [box][step] (per-box copies) or [step][box] (one copy).
+    const bool merged = p.tma3d >= kCopyMerged3d;
+    const uint32_t box_stride = merged ? kBoxBytes : spb * kBoxBytes;
+    const uint32_t step_bytes = merged ? BOXES * kBoxBytes : kBoxBytes;
     const uint32_t adv_stage = P::NCW / cps, adv_within = P::NCW - (P::NCW / cps) * cps;
     uint32_t c = warp;
     uint32_t within = c % cps;
@@ -835,10 +862,10 @@ __device__ void consumer_role(const typename P::Params& p, const Smem& S, const 
                 // the parity wait below refers to this stage's phase.
                 if (!__all_sync(0xffffffffu, wait_shared_value(bars.ring_tag(slot), stage, S.wait))) return;
                 if (!warp_wait(bars.full(slot), phase, S.wait)) return;
-                uint32_t step_smem = ring + slot * stage_bytes + within * G * kBoxBytes;
+                uint32_t step_smem = ring + slot * stage_bytes + within * G * step_bytes;
                 int kb = pl.kb0 + static_cast<int>((c - cb) * G);
                 const bool wide = *S.wide != 0;  // stable once this chunk's activations are staged
-                for (uint32_t st = 0; st < G; ++st, ++kb, step_smem += kBoxBytes) {
+                for (uint32_t st = 0; st < G; ++st, ++kb, step_smem += step_bytes) {
                     if (wide)
                         consume_step<NT, BOXES, true>(step_smem, box_stride, sc, p.nblk, kb, pl.kblk0, pl.kblk1,
                                                       ncols, xs_s, L.xs_stride, fx_s, L.fx_stride, acc, lane);
@@ -960,7 +987,9 @@ __device__ void consumer_parts(const typename P::Params& p, const Smem& S, const
     const Bars& bars = S.bars;
     const uint32_t spb = L.steps;
     const uint32_t stage_bytes = spb * BOXES * kBoxBytes;
-    const uint32_t box_stride = spb * kBoxBytes;
+    const bool merged = p.tma3d >= kCopyMerged3d;  // stage layout [step][box] instead of [box][step]
+    const uint32_t box_stride = merged ? kBoxBytes : spb * kBoxBytes;
+    const uint32_t step_bytes = merged ? BOXES * kBoxBytes : kBoxBytes;
     const uint32_t spi = L.part_steps / spb;  // stages per item
     uint8_t* xs = S.gbase + L.xs;
     uint8_t* fx = S.gbase + L.fx;
@@ -1045,7 +1074,7 @@ __device__ void consumer_parts(const typename P::Params& p, const Smem& S, const
                 if (!warp_wait(bars.full(slot), phase, S.wait)) return;
                 uint32_t step_smem = ring + slot * stage_bytes;
                 const bool wide = *S.wide != 0;  // stable once this part's activations are staged
-                for (uint32_t st = 0; st < spb; ++st, ++kb, step_smem += kBoxBytes) {
+                for (uint32_t st = 0; st < spb; ++st, ++kb, step_smem += step_bytes) {
                     if (wide)
                         consume_step<NT, BOXES, true>(step_smem, box_stride, sc, p.nblk, kb, kblk0, kblk1, ncols,
                                                       xcur, L.xs_stride, fcur, L.fx_stride, acc, lane);

@@ -289,8 +289,7 @@ int launch_ffn(const FfnArgs& a, int num_sms, int max_smem, cudaStream_t stream)
     down.layout = pl.down;
 
     CUtensorMap map1, map2;
-    if (int rc = encode_weights(&map1, a.w1q, 2 * static_cast<int64_t>(a.inter), a.hidden,
-                                static_cast<int>(pl.up.steps), &up.tma3d))
+    if (int rc = encode_weights_gate_up(&map1, a.w1q, 1, a.inter, a.hidden, static_cast<int>(pl.up.steps), &up.tma3d))
         return rc;
     if (int rc = encode_weights(&map2, a.w2q, a.hidden, a.inter, static_cast<int>(pl.down.steps), &down.tma3d))
         return rc;

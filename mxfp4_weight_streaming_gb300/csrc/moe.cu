@@ -487,11 +487,12 @@ int launch_moe(const uint8_t* w1q, const uint8_t* w2q, const MoeArgs& a, int num
         return MXFP4_ERR_SHAPE;
 
     CUtensorMap map1, map2;
-    if (int rc = encode_weights(&map1, w1q, Et * 2 * a.inter, a.hidden, static_cast<int>(g.layout.steps),
-                                &g.tma3d))
+    // One copy per stage: an expert's 16 gate rows with their 16 up rows, and
+    // 32 consecutive W2 rows.
+    if (int rc = encode_weights_gate_up(&map1, w1q, Et, a.inter, a.hidden, static_cast<int>(g.layout.steps), &g.tma3d))
         return rc;
-    if (int rc = encode_weights(&map2, w2q, Et * a.hidden, a.inter, static_cast<int>(d.layout.steps),
-                                &d.tma3d))
+    if (int rc = encode_weights_merged_rows(&map2, w2q, Et * a.hidden, a.inter, static_cast<int>(d.layout.steps), 32,
+                                            &d.tma3d))
         return rc;
 
     const int route_smem = static_cast<int>((P + 2 * Et) * 4);

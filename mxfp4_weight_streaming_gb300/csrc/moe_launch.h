@@ -27,7 +27,12 @@ size_t moe_workspace_bytes(int64_t t, int64_t e, int kp, int64_t hidden, int64_t
 int launch_moe(const uint8_t* w1q, const uint8_t* w2q, const MoeArgs& a, int num_sms, int max_smem,
                cudaStream_t stream);
 
-// Tensor map of packed weights [rows, k/2] (defined with the C ABI).
+// Tensor maps of packed weights [rows, k/2] (defined with the C ABI). The
+// int written is the engine's copy mode (Params::tma3d, see engine.cuh).
 int encode_weights(CUtensorMap* map, const uint8_t* wq, int64_t rows, int64_t k, int steps, int* is3d);
+int encode_weights_merged_rows(CUtensorMap* map, const uint8_t* wq, int64_t rows, int64_t k, int steps, int box_rows,
+                               int* mode);
+int encode_weights_gate_up(CUtensorMap* map, const uint8_t* w1q, int64_t experts, int64_t inter, int64_t k, int steps,
+                           int* mode);
 
 }  // namespace mxfp4

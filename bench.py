@@ -43,7 +43,8 @@ METRIC = "effective HBM GB/s (% of GB300 peak) and us/call, MXFP4 GEMM at T=1-32
 FALLBACK_HBM_GBS = 6800.0  # fallback peak when no measured peak file is present
 KERNEL_SOURCES = ["mxfp4_weight_streaming_gb300/csrc/linear.cu", "mxfp4_weight_streaming_gb300/csrc/engine.cuh",
                   "mxfp4_weight_streaming_gb300/csrc/engine_layout.h",
-                  "mxfp4_weight_streaming_gb300/csrc/device_common.cuh"]
+                  "mxfp4_weight_streaming_gb300/csrc/device_common.cuh",
+                  "mxfp4_weight_streaming_gb300/csrc/f4_linear.cu", "mxfp4_weight_streaming_gb300/csrc/tc_common.cuh"]
 
 WORKLOADS = {
     "linear_t1_k1024_n1024": dict(t=1, k=1024, n=1024, seed=0, x64=False),
@@ -203,6 +204,7 @@ PLAN_KERNELS = {
     1: "mxfp4::stream_kernel<DenseProblem, K in parts> (mma.sync)",
     2: "mxfp4::stream_kernel<DenseProblem, cluster split of K> (mma.sync)",
     3: "mxfp4::tc::tc_linear_kernel (tcgen05.mma kind::mxf8f6f4 block-scaled)",
+    4: "mxfp4::f4::f4_linear_kernel (tcgen05.mma kind::mxf4 block-scaled, packed E2M1 weights and digit pieces)",
 }
 
 

@@ -98,10 +98,22 @@ int mxfp4_quantize(const float* w, int64_t n, int64_t k, uint8_t* wq, uint8_t* w
  *   n   output features (>= 1, < 2^31)
  *   y   device bf16 [t, n], row-major, 2-byte aligned (output)
  * Accumulation is fp32 (tensor-core fp32 accumulate); the summation order
- * is the kernel's. Two kernels serve the call (mxfp4_linear_plan says which):
- *   - t <= 4, or k % 512 != 0, or wq not 32-byte aligned: the streaming
+ * is the kernel's. Three kernels serve the call (mxfp4_linear_plan says
+ * which):
+ *   - t <= 8 and k % 512 == 0: the packed-E2M1 tensor-core kernel
+ *     (tcgen05.mma kind::mxf4: the weight codes go from HBM to the tensor
+ *     cores as stored, two per byte, with their E8M0 scales). Its other
+ *     operand is E2M1 too, so each bf16 activation is written as eight
+ *     E2M1 digit pieces: with E = floor(log2) of the largest magnitude of
+ *     its (token, 32 values) block (at least -112), X = round(|x| 2^(15-E))
+ *     has eight 2-bit digits D_p (most significant first) and
+ *     x = sign * sum_p (D_p / 2) 2^(E - 2p). Exact for every value within
+ *     2^8 of its block's largest magnitude; smaller ones keep an absolute
+ *     error of at most 2^(E-16) (for blocks whose largest magnitude is
+ *     below 2^-112, at most 2^-128: the lowest piece scale is 2^-127).
+ *   - k % 512 != 0, or t >= 9 with wq not 32-byte aligned: the streaming
  *     engine (E2M1 -> f16 in registers, mma.sync, fp32 block scaling).
- *   - otherwise (5 <= t <= 32): the block-scaled tensor-core kernel
+ *   - otherwise (9 <= t <= 32): the block-scaled tensor-core kernel
  *     (tcgen05.mma kind::mxf8f6f4: the E2M1 codes and E8M0 scales go to
  *     the tensor cores as stored). Its other operand is 8-bit, so each bf16
  *     activation is split into two E4M3 pieces under one power-of-two scale
@@ -138,7 +150,9 @@ typedef struct {
     int32_t mode;        /* 0: whole K per CTA; 1: K walked in parts per CTA;
                             2: K split over a thread-block cluster (modes 0-2:
                             the streaming engine); 3: the block-scaled
-                            tensor-core kernel (cluster 2 = K split) */
+                            tensor-core kernel with E4M3 activation pieces;
+                            4: the packed-E2M1 tensor-core kernel (modes 3-4:
+                            cluster 2 = K split in halves) */
     int32_t ctas;        /* CTAs launched (mode 2: an upper bound; the number
                             of co-resident clusters decides) */
     int32_t cluster;     /* CTAs per cluster (1 unless mode 2) */
@@ -148,8 +162,11 @@ typedef struct {
     int32_t ring_slots;  /* stages in the weight ring */
     int32_t part_steps;  /* mode 1: K steps per part; else 0 */
     int32_t batch_units; /* mode 1: row groups of 16 rows per batch; mode 3:
-                            128-row tiles per CTA at most; else 0 */
+                            128-row tiles per CTA at most; mode 4: tiles of
+                            at most 128 rows per group; else 0 */
     int32_t smem_bytes;  /* dynamic shared memory per CTA */
+    int32_t group_rows;  /* mode 4: output rows per CTA (or per cluster), a
+                            multiple of 8; else 0 */
 } mxfp4_linear_plan_t;
 int mxfp4_linear_plan(int64_t t, int64_t k, int64_t n, int num_sms, int max_smem, mxfp4_linear_plan_t* out);
 

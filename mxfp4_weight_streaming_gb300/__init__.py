@@ -41,7 +41,8 @@ class Mxfp4Error(RuntimeError):
 class LinearPlan(ctypes.Structure):
     """mxfp4_linear_plan_t: how mxfp4_linear cuts the weight stream."""
     _fields_ = [(name, ctypes.c_int32) for name in ("mode", "ctas", "cluster", "stage_steps", "chunk_steps",
-                                                     "ring_slots", "part_steps", "batch_units", "smem_bytes")]
+                                                     "ring_slots", "part_steps", "batch_units", "smem_bytes",
+                                                     "group_rows")]
 
 
 PLAN_MODES = {0: "whole K", 1: "K in parts", 2: "cluster split of K"}

@@ -12,7 +12,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libmxfp4.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["quantize.cu", "linear.cu", "moe.cu", "capi.cu", "moe_noalloc.cu", "tc_linear.cu", "ffn.cu"]
+SOURCES = ["quantize.cu", "linear.cu", "moe.cu", "capi.cu", "moe_noalloc.cu", "tc_linear.cu", "ffn.cu", "f4_linear.cu"]
 NVCC = os.environ.get("NVCC", os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc"))
 FLAGS = ["-std=c++17", "-O3", "-lineinfo", "-gencode", "arch=compute_103a,code=sm_103a", "-Xcompiler", "-fPIC",
          "-Xcompiler", "-fvisibility=hidden",

@@ -13,6 +13,7 @@
 #include "ffn_launch.h"
 #include "moe_launch.h"
 #include "tc_linear_launch.h"
+#include "f4_linear_launch.h"
 #include "mxfp4.h"
 
 namespace {
@@ -112,6 +113,21 @@ int encode_tc_weight_map(CUtensorMap* map, const uint8_t* wq, int64_t rows, int6
     return r == CUDA_SUCCESS ? MXFP4_OK : MXFP4_ERR_CUDA;
 }
 
+// Packed weights [rows, k/2] for the packed-E2M1 tensor-core kernel: the 3D
+// view (128 B, rows, k/256) with strides (k/2 B, 128 B) and a box of 2
+// atoms x box_rows rows, so one copy lands [atom][row][128 B] swizzled, the
+// codes as stored. Needs k % 512 == 0.
+int encode_f4_weight_map(CUtensorMap* map, const uint8_t* wq, int64_t rows, int64_t k, int box_rows) {
+    cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(k / 256)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(k / 2), 128};
+    cuuint32_t box[3] = {128, static_cast<cuuint32_t>(box_rows), 2};
+    cuuint32_t estride[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(wq), dims, strides, box,
+                          estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MXFP4_OK : MXFP4_ERR_CUDA;
+}
+
 }  // namespace
 
 namespace mxfp4 {
@@ -182,10 +198,12 @@ struct LinearPlan {
     const uint8_t* wq = nullptr;
     const uint8_t* ws = nullptr;
     int64_t t = 0, k = 0, n = 0;
-    bool tc = false;  // block-scaled tensor-core kernel (else the streaming engine)
+    int kind = 0;  // 0: streaming engine; 1: E4M3-split tensor-core kernel; 2: packed-E2M1 tensor-core kernel
     mxfp4::LinearParams p{};
     mxfp4::tc::TcPlan tp{};
+    mxfp4::f4::F4Plan fp{};
     CUtensorMap map;
+    CUtensorMap tail_map;  // kind 2 with a tail tile
 };
 constexpr int kPlanCache = 16;
 thread_local LinearPlan t_plans[kPlanCache];
@@ -253,10 +271,18 @@ int mxfp4_linear(const void* x, int64_t t, int64_t k, const uint8_t* wq, const u
         }
     if (!plan) {
         LinearPlan fresh;
-        // The block-scaled tensor-core kernel when the shape and the weight
+        // t <= 8: the packed-E2M1 tensor-core kernel when k % 512 == 0. Then
+        // the E4M3-split tensor-core kernel when the shape and the weight
         // alignment allow it; the streaming engine otherwise.
-        fresh.tc = aligned(wq, 32) && mxfp4::tc::plan_tc(static_cast<int>(t), k, n, d->num_sms, d->max_smem, &fresh.tp);
-        if (fresh.tc) {
+        if (mxfp4::f4::plan_f4(static_cast<int>(t), k, n, d->num_sms, d->max_smem, &fresh.fp)) {
+            fresh.kind = 2;
+            if (int rc = encode_f4_weight_map(&fresh.map, wq, n, k, fresh.fp.h_main)) return rc;
+            fresh.tail_map = fresh.map;
+            if (fresh.fp.h_tail)
+                if (int rc = encode_f4_weight_map(&fresh.tail_map, wq, n, k, fresh.fp.h_tail)) return rc;
+        } else if (aligned(wq, 32) &&
+                   mxfp4::tc::plan_tc(static_cast<int>(t), k, n, d->num_sms, d->max_smem, &fresh.tp)) {
+            fresh.kind = 1;
             if (int rc = encode_tc_weight_map(&fresh.map, wq, n, k, fresh.tp.atoms_per_stage)) return rc;
         } else {
             if (!linear_plan(t, k, n, d->num_sms, d->max_smem, &fresh.p.cl, &fresh.p.layout)) return MXFP4_ERR_SHAPE;
@@ -275,7 +301,31 @@ int mxfp4_linear(const void* x, int64_t t, int64_t k, const uint8_t* wq, const u
         *plan = fresh;
     }
     const CUtensorMap& map = plan->map;
-    if (plan->tc) {
+    if (plan->kind == 2) {
+        const mxfp4::f4::F4Plan& fp = plan->fp;
+        mxfp4::f4::F4Params q{};
+        q.x = static_cast<const __nv_bfloat16*>(x);
+        q.ws = ws;
+        q.y = static_cast<__nv_bfloat16*>(y);
+        q.status = d->status;
+        q.T = static_cast<int>(t);
+        q.K = static_cast<int>(k);
+        q.N = static_cast<int>(n);
+        q.nblk = static_cast<int>(k / 32);
+        q.stages = static_cast<int>(k / 512);
+        q.rows = fp.rows;
+        q.h_main = fp.h_main;
+        q.h_tail = fp.h_tail;
+        q.cl = fp.cl;
+        q.na = fp.na;
+        q.nb = fp.nb;
+        q.max_batch = fp.max_batch;
+        q.tmem_cols = fp.tmem_cols;
+        q.inbox_bytes = fp.cl > 1 ? fp.tiles * q.T * 128 * 4 : 0;
+        cudaError_t e = mxfp4::f4::launch_f4_linear(map, plan->tail_map, q, fp, static_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
+    }
+    if (plan->kind == 1) {
         mxfp4::tc::TcLinearParams q{};
         q.x = static_cast<const __nv_bfloat16*>(x);
         q.ws = ws;
@@ -310,6 +360,22 @@ int mxfp4_linear(const void* x, int64_t t, int64_t k, const uint8_t* wq, const u
 int mxfp4_linear_plan(int64_t t, int64_t k, int64_t n, int num_sms, int max_smem, mxfp4_linear_plan_t* out) {
     if (!out || num_sms <= 0 || max_smem <= 0) return MXFP4_ERR_INVALID_ARG;
     if (int rc = linear_shape_status(t, k, n)) return rc;
+    mxfp4::f4::F4Plan fp{};
+    if (mxfp4::f4::plan_f4(static_cast<int>(t), k, n, num_sms, max_smem, &fp)) {
+        mxfp4_linear_plan_t r{};
+        r.mode = 4;
+        r.ctas = fp.grid;
+        r.cluster = fp.cl;
+        r.stage_steps = 2;  // 512 K values per stage
+        r.chunk_steps = 2;
+        r.ring_slots = fp.na;
+        r.part_steps = 0;
+        r.batch_units = fp.tiles;  // tiles of at most 128 rows per group
+        r.smem_bytes = fp.smem_bytes;
+        r.group_rows = fp.rows;
+        *out = r;
+        return MXFP4_OK;
+    }
     mxfp4::tc::TcPlan tp{};
     if (mxfp4::tc::plan_tc(static_cast<int>(t), k, n, num_sms, max_smem, &tp)) {
         mxfp4_linear_plan_t r{};

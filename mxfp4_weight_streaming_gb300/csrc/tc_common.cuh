@@ -95,6 +95,23 @@ __device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, u
         : "memory");
 }
 
+// Both operands packed E2M1 (two codes per byte, the even K index in the low
+// nibble, as stored in HBM): D[128 x N] (+)= A[128 x 64] * B[N x 64]^T with
+// one E8M0 scale per 32 values on each side (scale_vec::2X). The scale ID of
+// the instruction descriptor picks bytes {0,1} (ID 0) or {2,3} (ID 2) of the
+// 32-bit TMEM scale word, whose 4 bytes cover 128 consecutive K values.
+constexpr uint32_t kFmtMxf4E2M1 = 1;
+
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(static_cast<uint32_t>(accumulate))
+        : "memory");
+}
+
 // Copy a 512-byte scale image from shared memory into 4 TMEM columns of all
 // 128 lanes (each 32-lane quarter gets the same 32 lines).
 __device__ __forceinline__ void copy_scales_to_tmem(uint32_t taddr, uint64_t sdesc) {

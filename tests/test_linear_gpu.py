@@ -3,10 +3,11 @@
 Packing is compared byte for byte; outputs elementwise under the stated
 bound |y - y_ref| <= 4e-3*|y_ref| + 1e-3*sqrt(sum_k (x_k*w_k)^2).
 
-mxfp4_linear has two kernels: the block-scaled tensor-core kernel for
-t >= 5 and k % 512 == 0 (plan mode 3) and the streaming engine otherwise
-(modes 0-2). Shapes below cover both; k % 512 != 0 twins keep the engine's
-whole-K, K-in-parts and cluster modes under test at t >= 5.
+mxfp4_linear has three kernels: the packed-E2M1 tensor-core kernel for
+t <= 8 and k % 512 == 0 (plan mode 4), the E4M3-split tensor-core kernel
+for t >= 9 and k % 512 == 0 (mode 3) and the streaming engine otherwise
+(modes 0-2). Shapes below cover all three; k % 512 != 0 twins keep the
+engine's whole-K, K-in-parts and cluster modes under test.
 """
 import numpy as np
 import pytest
@@ -163,13 +164,14 @@ def test_linear_odd_stage_sizes_sampled(t, k, n):
 
 @pytest.mark.parametrize("t,k,n", [(1, 262144, 40), (32, 262144, 24), (1, 262112, 40), (32, 262112, 24)])
 def test_linear_largest_k(t, k, n):
-    """The largest k the header promises (262144). Tensor-core kernel: one
-    tile shared by a 2-CTA cluster, 256 stages per CTA. Streaming engine
+    """The largest k the header promises (262144). Tensor-core kernels: one
+    tile per 2-CTA cluster, 256 stages per CTA (t = 1: packed E2M1, groups
+    of 8 rows; t = 32: E4M3 split). Streaming engine
     (k = 262112): one row group's scales for all of k take 128 KB of shared
     memory, so each CTA walks K in parts (hundreds of them) with a single
     row group; ragged last row group."""
     mx = lib()
-    assert mx.linear_plan(t, k, n)["mode"] == (3 if k % 512 == 0 and t >= 5 else 1)
+    assert mx.linear_plan(t, k, n)["mode"] == ((4 if t <= 8 else 3) if k % 512 == 0 else 1)
     w, x = linear_case(110 + t, t, k, n)
     wq, ws, rq, rs = _pack_both(w)
     y = mx.linear(x, wq, ws)
@@ -192,8 +194,8 @@ def test_linear_config1_full():
 
 @pytest.mark.parametrize("t", [4, 8])
 def test_linear_verify_full(t):
-    """K=N=7168, whole output: T=4 (one target + three drafts; streaming
-    engine) and T=8 (tensor-core kernel, 2-CTA clusters)."""
+    """K=N=7168, whole output: T=4 (one target + three drafts) and T=8, both
+    on the packed-E2M1 kernel (75 clusters of 2 CTAs, 96 rows each)."""
     mx = lib()
     w, x = linear_case(1, t, 7168, 7168)
     wq, ws, rq, rs = _pack_both(w)
@@ -206,8 +208,9 @@ def test_linear_verify_full(t):
 
 @pytest.mark.parametrize("t", [4, 6])
 def test_linear_lmhead_full_size_sampled(t):
-    """LM head K=7168, N=129280 with 1% of blocks x64 (T=4 as configured;
-    T=6 runs the tensor-core kernel, 6-7 tiles per CTA in one batch):
+    """LM head K=7168, N=129280 with 1% of blocks x64 (T=4 as configured,
+    and T=6): the packed-E2M1 kernel, 856 rows per CTA in six 128-row tiles
+    and one of 88 rows, one batch; the last CTA holds 24 rows):
     packing of sampled rows bit-exact, sampled output rows within tolerance."""
     mx = lib()
     k, n = 7168, 129280
@@ -245,8 +248,8 @@ def test_linear_ffn_sweep_sampled(t):
 @pytest.mark.parametrize("t,k", [(5, 512), (3, 512), (3, 544)])
 def test_linear_extreme_scales(t, k):
     """Blocks with scale bytes 0, 1, 2, 250, 252 and 254 next to ordinary ones;
-    activations chosen so every exact output stays inside bf16 range (both
-    kernels: t = 5, k = 512 tensor core; t = 3 streaming engine)."""
+    activations chosen so every exact output stays inside bf16 range (t = 5
+    and t = 3 at k = 512: packed-E2M1 kernel; k = 544: streaming engine)."""
     mx = lib()
     rng = np.random.default_rng(5)
     n = 64
@@ -271,7 +274,7 @@ def test_linear_extreme_scales(t, k):
 @pytest.mark.parametrize("t,k", [(4, 1024), (6, 1024), (6, 1056)])
 def test_linear_activation_extremes(t, k):
     """bf16 activations spanning subnormal to 2^120, and all-zero blocks
-    (both kernels: t = 6, k = 1024 tensor core)."""
+    (k = 1024: packed-E2M1 kernel; k = 1056: streaming engine)."""
     mx = lib()
     rng = np.random.default_rng(6)
     n = 96
@@ -313,15 +316,17 @@ def test_linear_scale_times_activation_factor_no_overflow(t, k):
     a zero code. The exact result is finite, but the weight scale times the
     activation block's own power-of-two factor reaches 2^128: no kernel may
     form that product on its way to the result. The large activation is 2^8
-    (tensor-core kernel, t = 6: its activation scale is 2^1) and 2^16
-    (streaming engine, t = 2: its staging factor is 2^2); the small ones
+    (E4M3-split kernel: its activation scale is 2^1) and 2^16 (streaming
+    engine, k = 544: its staging factor is 2^2); the small ones
     are +-2^-5 times a 4-bit significand, so every piece of them stays
     exact, and the weight codes of the block are +-0.5, which keeps every
-    exact output below 2^127."""
+    exact output below 2^127. On the packed-E2M1 kernel (k = 512) the large
+    activation is 2^2: its digit pieces hold values down to 2^-13 exactly,
+    and the weight scale times the top piece's scale is 2^129."""
     mx = lib()
     rng = np.random.default_rng(12)
     n = 48
-    big = 2.0 ** 8 if mx.linear_plan(t, k, n)["mode"] == 3 else 2.0 ** 16
+    big = {3: 2.0 ** 8, 4: 2.0 ** 2}.get(mx.linear_plan(t, k, n)["mode"], 2.0 ** 16)
     rq = rng.integers(0, 256, (n, k // 2), dtype=np.uint8)
     rs = rng.integers(120, 126, (n, k // 32), dtype=np.uint8)
     xs = rng.normal(0, 1, (t, k)).astype(np.float32)
@@ -345,3 +350,55 @@ def test_linear_scale_times_activation_factor_no_overflow(t, k):
     yg = bf16_to_f64(y)
     assert np.all(np.isfinite(yg)), "overflow"
     assert_within(yg, y_ref, rss, f"scale x factor, k={k}")
+
+
+@pytest.mark.parametrize("t,k", [(1, 1024), (4, 2048), (8, 1024)])
+def test_linear_digit_pieces_exact(t, k):
+    """Packed-E2M1 kernel: one weight of 1.0 per row (code 2, scale 2^0)
+    makes y[t][n] = x[t][k_n], so y shows each activation as the kernel's
+    digit pieces rebuild it. Within 2^8 of its block's largest magnitude a
+    bf16 activation is rebuilt exactly, so y equals x bit for bit; further
+    below, the error is at most 2^(E-16) (E = floor(log2) of the block
+    maximum), and the oracle's tolerance holds for every output."""
+    mx = lib()
+    n = 2 * k // 32
+    assert mx.linear_plan(t, k, n)["mode"] == 4
+    rng = np.random.default_rng(13)
+    # Activations: per 32-block one magnitude 2^e0 and elements spread over
+    # 2^e0 .. 2^(e0 - 12); one all-zero block. (Block maxima stay above
+    # 2^-112: the lowest piece scale is 2^-127, so smaller blocks lose their
+    # values below 2^-128.)
+    e0 = rng.integers(-100, 100, (t, k // 32)).repeat(32, axis=1)
+    xs = rng.choice([-1.0, 1.0], (t, k)) * (1 + rng.random((t, k))) * 2.0 ** (e0 - rng.integers(0, 13, (t, k)))
+    xs[:, 0:32] = 0.0
+    x = torch.from_numpy(xs.astype(np.float32)).to(torch.bfloat16)
+    xf = x.double().numpy()
+    # Row r selects k_r: two rows per block (a large and a small element).
+    kr = np.empty(n, np.int64)
+    for b in range(k // 32):
+        mags = np.abs(xf[0, 32 * b:32 * b + 32])
+        kr[2 * b] = 32 * b + int(np.argmax(mags))
+        kr[2 * b + 1] = 32 * b + int(np.argmin(np.where(mags > 0, mags, np.inf))) if (mags > 0).any() else 32 * b
+    codes = np.zeros((n, k), np.uint8)
+    codes[np.arange(n), kr] = 2  # 1.0
+    rq = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    rs = np.full((n, k // 32), 127, np.uint8)
+    y = mx.linear(x.cuda(), torch.from_numpy(rq).cuda(), torch.from_numpy(rs).cuda())
+    torch.cuda.synchronize()
+    yg = bf16_to_f64(y)
+    y_ref, rss = oracle.linear(x, rq, rs)
+    sel = xf[:, kr]  # [t, n]: the selected activation of each output
+    assert np.array_equal(y_ref, sel)
+    blk_max = np.abs(xf).reshape(t, k // 32, 32).max(axis=2)[:, kr // 32]
+    near = (np.abs(sel) * 2.0 ** 8 >= blk_max) | (sel == 0)
+    assert near.any() and (~near).any()
+    assert np.array_equal(yg[near], sel[near]), "values within 2^8 of the block maximum are exact"
+    # (A one-hot row's tolerance is 5e-3 of the value itself, tighter than
+    # the split's bound for elements far below their block maximum; those
+    # are checked against the bound below instead.)
+    assert_within(yg[near], y_ref[near], rss[near], "digit pieces")
+    e_blk = np.floor(np.log2(np.where(blk_max > 0, blk_max, 1.0)))
+    bound = 2.0 ** (np.maximum(e_blk, -112) - 16)
+    # y is the rebuilt value rounded to bf16: at most the piece error plus half a bf16 ulp of it.
+    err = np.abs(yg - sel)
+    assert np.all(err[~near] <= bound[~near] + np.abs(sel[~near]) * 2.0 ** -8)

@@ -1,8 +1,9 @@
 """The launch plans of mxfp4_linear, checked on the host (no GPU): which
-kernel a shape gets (the block-scaled tensor-core kernel when t >= 5 and
-k % 512 == 0, else the streaming engine with whole K per CTA, K walked in
-parts or a cluster split of K), and the invariants every plan must keep for
-the kernel's indexing to hold."""
+kernel a shape gets (the packed-E2M1 tensor-core kernel when t <= 8 and
+k % 512 == 0, the E4M3-split tensor-core kernel when t >= 9 and k % 512 ==
+0, else the streaming engine with whole K per CTA, K walked in parts or a
+cluster split of K), and the invariants every plan must keep for the
+kernel's indexing to hold."""
 import math
 
 import pytest
@@ -23,12 +24,28 @@ def consumer_warps(t):
     return 14 if t <= 8 else (12 if t <= 16 else 8)
 
 
+@pytest.mark.parametrize("t,k,n,cluster,ctas,rows,tiles", [
+    (4, 7168, 7168, 2, 150, 96, 1),       # verify: 75 clusters of 96 rows, K in halves
+    (8, 7168, 7168, 2, 150, 96, 1),
+    (1, 1024, 1024, 2, 128, 16, 1),       # 64 clusters of 16 rows
+    (1, 7168, 18432, 1, 144, 128, 1),     # FFN up: one 128-row tile per CTA
+    (8, 7168, 18432, 1, 144, 128, 1),
+    (4, 7168, 129280, 1, 152, 856, 7),    # LM head: 6 tiles of 128 rows and one of 88 per CTA
+    (3, 512, 64, 1, 8, 8, 1),             # one stage: no K split, 8-row groups
+])
+def test_packed_e2m1_plans(t, k, n, cluster, ctas, rows, tiles):
+    p = mx.linear_plan(t, k, n, SMS, SMEM)
+    assert p["mode"] == 4, p
+    assert (p["cluster"], p["ctas"], p["group_rows"], p["batch_units"]) == (cluster, ctas, rows, tiles), p
+    assert p["stage_steps"] == 2 and p["part_steps"] == 0 and p["ring_slots"] >= 2, p
+
+
 @pytest.mark.parametrize("t,k,n,cluster,ctas", [
-    (8, 7168, 7168, 2, 112),        # 56 tiles of 128 rows, K split over 2-CTA clusters
-    (5, 1024, 1024, 2, 16),
-    (8, 7168, 18432, 1, 144),       # FFN up: one tile per CTA
+    (9, 7168, 7168, 2, 112),        # 56 tiles of 128 rows, K split over 2-CTA clusters
+    (9, 1024, 1024, 2, 16),
+    (16, 7168, 18432, 1, 144),      # FFN up: one tile per CTA
     (32, 7168, 18432, 1, 144),
-    (6, 7168, 129280, 1, 152),      # LM-head width: 1010 tiles over every SM
+    (12, 7168, 129280, 1, 152),     # LM-head width: 1010 tiles over every SM
     (16, 7168, 4900, 2, 78),
 ])
 def test_tensor_core_plans(t, k, n, cluster, ctas):
@@ -41,13 +58,12 @@ def test_tensor_core_plans(t, k, n, cluster, ctas):
 
 
 @pytest.mark.parametrize("t,k,n,mode,stage,chunk,part,batch", [
-    (4, 7168, 7168, 0, 4, 4, 0, 0),      # t <= 4: streaming engine; verify: 3 row groups per CTA, 4-step stages
-    (1, 1024, 1024, 0, 4, 1, 0, 0),      # one row group of 4 steps per CTA: 1-step chunks
-    (1, 7168, 18432, 0, 7, 7, 0, 0),     # FFN up, whole-stage chunks
-    (4, 7168, 129280, 0, 7, 7, 0, 0),    # LM head
     (4, 7200, 7168, 0, 1, 1, 0, 0),      # k % 512 != 0: 29 K steps (prime): 1-step stages
     (1, 1056, 1024, 0, 1, 1, 0, 0),      # 5 K steps, the last one block long
+    (4, 7424, 7168, 0, 1, 1, 0, 0),      # 29 K steps of 256
+    (1, 7424, 18432, 0, 1, 1, 0, 0),
     (8, 6176, 18432, 0, 5, 5, 0, 0),     # 25 K steps: whole 5-step stage chunks
+    (2, 6400, 129280, 0, 5, 5, 0, 0),    # 25 K steps, LM-head width
     (32, 7200, 18432, 1, 1, 1, 1, 8),    # activations of all of K fill shared memory: K in parts
     (32, 7200, 4900, 1, 1, 1, 1, 3),     # 29 K steps (prime): one-step parts
 ])
@@ -83,18 +99,31 @@ def test_plan_invariants_over_shapes():
         seen.add(p["mode"])
         where = f"t={t} k={k} n={n}: {p}"
         assert p["smem_bytes"] <= SMEM, where
+        if p["mode"] == 4:
+            # packed-E2M1 kernel: t <= 8, k % 512; groups of a multiple of 8
+            # rows covering n, one per CTA or per 2-CTA cluster (K halves,
+            # only when lone CTAs would get < 96 rows and K has >= 2 stages)
+            assert k % 512 == 0 and t <= 8, where
+            rows, cl = p["group_rows"], p["cluster"]
+            lone_rows = -(-(-(-n // SMS)) // 8) * 8
+            assert cl == (2 if lone_rows < 96 and k >= 1024 else 1), where
+            assert rows % 8 == 0 and rows >= 8 and p["ctas"] == cl * -(-n // rows) <= SMS, where
+            assert p["ctas"] // cl * rows >= n > (p["ctas"] // cl - 1) * rows, where
+            assert p["batch_units"] == (1 if rows <= 128 else rows // 128 + (rows % 128 != 0)), where
+            assert p["stage_steps"] == 2 and p["ring_slots"] >= 2, where
+            continue
         if p["mode"] == 3:
             # tensor-core kernel: t >= 5, k % 512, 128-row tiles, one tile
             # per 2-CTA cluster or a tile range per CTA, 2- or 4-atom stages
             tiles = -(-n // 128)
-            assert k % 512 == 0 and t >= 5, where
+            assert k % 512 == 0 and t >= 9, where
             assert p["stage_steps"] in (1, 2) and p["ring_slots"] >= 2, where
             if p["cluster"] == 2:
                 assert p["ctas"] == 2 * tiles and 2 * tiles <= SMS and p["batch_units"] == 1, where
             else:
                 assert p["cluster"] == 1 and p["ctas"] == min(SMS, tiles), where
             continue
-        assert k % 512 != 0 or t <= 4, where
+        assert k % 512 != 0, where
         nkb = -(-k // 256)
         n_rg = -(-n // 16)
         upc = -(-n_rg // min(SMS, n_rg))
@@ -121,7 +150,7 @@ def test_plan_invariants_over_shapes():
             steps = [min(nkb, (r + 1) * share) - min(nkb, r * share) for r in range(cl)]
             assert all(s % p["stage_steps"] == 0 for s in steps), where
             assert p["part_steps"] == 0 and p["batch_units"] == 0, where
-    assert seen == {0, 1, 2, 3}
+    assert seen == {0, 1, 2, 3, 4}
 
 
 def test_plan_argument_errors():

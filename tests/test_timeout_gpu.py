@@ -8,8 +8,8 @@ no arrival made - and a 1 ms limit, so the consumers' wait on that stage
 runs out. The call must report MXFP4_ERR_TIMEOUT through
 mxfp4_last_device_status, leave the context usable, and the product library
 must then give oracle-exact results. Cases: the streaming engine with lone
-CTAs, and the tensor-core kernel both with lone CTAs and with 2-CTA
-clusters (rank 0 times out while rank 1 hands it partials).
+CTAs, and both tensor-core kernels (E4M3 split, packed E2M1) with lone CTAs
+and with 2-CTA clusters (rank 0 times out while rank 1 hands it partials).
 """
 import ctypes
 
@@ -37,7 +37,8 @@ def withhold_lib():
     return L
 
 
-@pytest.mark.parametrize("t,k,n,mode,cluster", [(2, 1024, 256, 0, 1), (8, 1024, 10240, 3, 1), (8, 4096, 256, 3, 2)])
+@pytest.mark.parametrize("t,k,n,mode,cluster", [(2, 1056, 256, 0, 1), (12, 1024, 10240, 3, 1), (12, 4096, 256, 3, 2),
+                                               (4, 1024, 20480, 4, 1), (4, 4096, 256, 4, 2)])
 def test_bounded_wait_runs_out_and_context_survives(withhold_lib, t, k, n, mode, cluster):
     mx = lib()
     plan = mx.linear_plan(t, k, n)

@@ -321,7 +321,7 @@ int mxfp4_linear(const void* x, int64_t t, int64_t k, const uint8_t* wq, const u
         q.nb = fp.nb;
         q.max_batch = fp.max_batch;
         q.tmem_cols = fp.tmem_cols;
-        q.inbox_bytes = fp.cl > 1 ? fp.tiles * q.T * 128 * 4 : 0;
+        q.inbox_bytes = fp.inbox_bytes;
         cudaError_t e = mxfp4::f4::launch_f4_linear(map, plan->tail_map, q, fp, static_cast<cudaStream_t>(stream));
         return e == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
     }

@@ -488,6 +488,18 @@ __device__ __forceinline__ void store_a_scale_words(uint32_t taddr, int q, const
     fence_before_sync();
 }
 
+// 16-byte vectors per inbox row: the tokens' sums (NPAD / 8 of them) in
+// groups of 4.
+__host__ __device__ constexpr int inbox_vectors(int npad) { return (npad / 8 + 3) / 4; }
+
+// Asynchronous store of 16 bytes into a peer CTA's shared memory, counted
+// as transaction bytes on the peer's mbarrier (cluster addresses).
+__device__ __forceinline__ void st_async_v4(uint32_t dst, float a, float b, float c, float d, uint32_t bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(dst),
+                 "f"(a), "f"(b), "f"(c), "f"(d), "r"(bar)
+                 : "memory");
+}
+
 // 16-byte global -> shared copy through L2 on the load/store path; with
 // src_bytes = 0 it writes zeros and reads nothing.
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
@@ -591,9 +603,8 @@ __device__ void epilogue_body(const F4Params& p, int q, int lane, const Work& w,
         }
         if (p.cl > 1 && !sender) {
             // One batch per group when K is split: rank 1's sums of every
-            // tile arrive together.
+            // tile arrive together, counted in bytes on the inbox barrier.
             if (!__all_sync(0xffffffffu, mbar_wait(bars.inbox(), 0, wc))) return;
-            fence_acq_rel_cluster();
         }
         for (int ti = t0; ti < t0 + bt; ++ti) {
             // 16 accumulator columns (two tokens) at a time keeps the
@@ -612,19 +623,32 @@ __device__ void epilogue_body(const F4Params& p, int q, int lane, const Work& w,
                     s[2 * c + h] = a;
                 }
             }
-            const uint32_t slot_off = static_cast<uint32_t>(((ti - t0) * T) * kTileRows + rt) * 4u;
+            // Inbox row of (tile, row): the sums of tokens 4v..4v+3 in its
+            // 16-byte vector v (kInboxVec of them).
+            constexpr int NV = inbox_vectors(NPAD);
+            const uint32_t row_off = static_cast<uint32_t>(((ti - t0) * kTileRows + rt) * NV * 16);
             if (sender) {
-                // Hand the fp32 sums to rank 0's inbox.
-                const uint32_t dst = map_to_rank(inbox, 0) + slot_off;
+                // Hand the fp32 sums to rank 0: asynchronous remote stores
+                // that count their bytes on rank 0's inbox barrier.
+                const uint32_t dst = map_to_rank(inbox, 0) + row_off;
+                const uint32_t rbar = map_to_rank(bars.inbox(), 0);
 #pragma unroll
-                for (int t = 0; t < NPAD / 8; ++t)
-                    if (t < T) st_cluster_f32(dst + t * kTileRows * 4, s[t]);
+                for (int v = 0; v < NV; ++v)
+                    st_async_v4(dst + 16 * v, s[4 * v], 4 * v + 1 < NPAD / 8 ? s[4 * v + 1] : 0.f,
+                                4 * v + 2 < NPAD / 8 ? s[4 * v + 2] : 0.f, 4 * v + 3 < NPAD / 8 ? s[4 * v + 3] : 0.f,
+                                rbar);
                 continue;
             }
             if (p.cl > 1) {
 #pragma unroll
-                for (int t = 0; t < NPAD / 8; ++t)
-                    if (t < T) s[t] += __uint_as_float(lds_u32_volatile(inbox + slot_off + t * kTileRows * 4));
+                for (int v = 0; v < NV; ++v) {
+                    const uint4 in = lds128(inbox + row_off + 16 * v);
+                    const float f4v[4] = {__uint_as_float(in.x), __uint_as_float(in.y), __uint_as_float(in.z),
+                                          __uint_as_float(in.w)};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if (4 * v + e < NPAD / 8) s[4 * v + e] += f4v[e];
+                }
             }
             const int row = w.tile_row0(ti) + rt;
             if (rt < tile_height(p, w, ti) && row < p.N) {
@@ -632,11 +656,6 @@ __device__ void epilogue_body(const F4Params& p, int q, int lane, const Work& w,
                 for (int t = 0; t < NPAD / 8; ++t)
                     if (t < T) p.y[static_cast<size_t>(t) * p.N + row] = __float2bfloat16_rn(s[t]);
             }
-        }
-        if (sender) {
-            fence_acq_rel_cluster();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive_remote(map_to_rank(bars.inbox(), 0));
         }
         fence_before_sync();
         __syncwarp();
@@ -709,10 +728,13 @@ __global__ void __launch_bounds__(kThreads, NPAD <= 32 ? 2 : 1)
         }
         mbar_init(bars.acc_full(), 1);
         mbar_init(bars.acc_empty(), kEpilogueWarps);
-        mbar_init(bars.inbox(), static_cast<uint32_t>((p.cl > 1 ? p.cl - 1 : 1) * kEpilogueWarps));
+        mbar_init(bars.inbox(), 1);
         mbar_init(bars.drain(), 1);
         *abort_flag = 0;
         fence_barrier_init();
+        // Rank 0 of a cluster expects rank 1's sums of every tile, in bytes
+        // (rank 1 sends only after the cluster barrier, so this comes first).
+        if (p.cl > 1 && w.rank == 0) mbar_arrive_expect_tx(bars.inbox(), static_cast<uint32_t>(p.inbox_bytes));
     }
     // Rows past 8T of the B buffers (padding of the MMA's N) and their scale
     // bytes are zero for the whole kernel; the converters never write them.
@@ -827,7 +849,7 @@ static bool plan_fit(int npad, int cl, int t, int64_t rows, int64_t groups, int 
     const int h_main = static_cast<int>(rows < kTileRows ? rows : kTileRows);
     const int h_tail = rows > kTileRows ? static_cast<int>(rows % kTileRows) : 0;
     const int tiles = rows <= kTileRows ? 1 : static_cast<int>(rows / kTileRows) + (h_tail ? 1 : 0);
-    const int inbox = cl > 1 ? tiles * t * kTileRows * 4 : 0;
+    const int inbox = cl > 1 ? tiles * kTileRows * inbox_vectors(npad) * 16 : 0;
     const int sfa_col = (cols - 16 * na - 16 * nb) / 32 * 32;
     const int max_batch = sfa_col / npad;
     if (max_batch < 1 || (cl > 1 && max_batch < tiles)) return false;
@@ -847,6 +869,7 @@ static bool plan_fit(int npad, int cl, int t, int64_t rows, int64_t groups, int 
     r.nb = nb;
     r.max_batch = max_batch;
     r.tmem_cols = cols;
+    r.inbox_bytes = inbox;
     r.smem_bytes = bytes;
     *out = r;
     return true;

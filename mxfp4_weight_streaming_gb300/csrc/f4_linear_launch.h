@@ -27,7 +27,7 @@ struct F4Params {
     int nb;         // activation (digit piece) buffers
     int max_batch;  // tiles whose accumulators fit in TMEM at once
     int tmem_cols;  // TMEM columns the CTA allocates (256 or 512)
-    int inbox_bytes;  // rank 0's inbox for rank 1's sums (cluster of 2: tiles x T x 128 x 4), else 0
+    int inbox_bytes;  // rank 0's inbox for rank 1's sums (cluster of 2: tiles x 128 rows x 16-byte vectors), else 0
 };
 
 // How a call is cut (host only).
@@ -43,6 +43,7 @@ struct F4Plan {
     int nb;          // activation buffers
     int max_batch;
     int tmem_cols;
+    int inbox_bytes;
     int smem_bytes;  // dynamic shared memory per CTA, as launched
 };
 

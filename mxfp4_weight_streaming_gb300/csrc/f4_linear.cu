@@ -349,62 +349,95 @@ __device__ __forceinline__ void transpose_nibbles(uint32_t (&s)[8]) {
     }
 }
 
-// One lane's 8 consecutive activations of a 32-value block (one 16-byte
-// load; word q holds elements 2q (low half) and 2q + 1). The block is held
-// by the 4 lanes l with l >> 2 == blk (j = l & 3 holds elements 8j..8j+7).
-// Writes the lane's 4-byte word of each of token t's 8 piece rows (rows
-// 8t + p of the swizzled B atom, 16-byte chunk blk) and the scale bytes of
-// pieces 2j and 2j + 1 (image row 8t + p, byte sbyte0 of the row).
-__device__ __forceinline__ void convert_unit(const uint4& v, int t, int blk, int j, uint32_t atom, uint32_t img,
-                                             int sbyte0) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t a[4];
+// Stores the 4-byte word of piece P of a lane's 8 elements: B row 8t + P
+// (row % 8 == P), swizzled 16-byte chunk blk ^ P. With base = row 8t's
+// address plus blk << 4 (bits 4-6) and 4j, the address is one XOR of bits
+// 4-6 and an immediate row offset.
+template <int P>
+__device__ __forceinline__ void store_piece(uint32_t base, uint32_t v) {
+    asm volatile("st.shared.u32 [%0+%2], %1;" ::"r"(base ^ (P << 4)), "r"(v), "n"(P * 128) : "memory");
+}
+
+// The units of one converter warp in one stage, converted in lockstep (each
+// step for all of them before the next, so their dependent chains overlap).
+// Unit u holds one lane's 8 consecutive activations of a 32-value block (one
+// 16-byte load; word q holds elements 2q (low half) and 2q + 1) of token
+// t0 + 2u; the block is held by the 4 lanes l with l >> 2 == blk (j = l & 3
+// holds elements 8j..8j+7). Units u < nun are written: the lane's word of
+// each of the token's 8 piece rows of the swizzled B atom, and the scale
+// bytes of pieces 2j and 2j + 1 (image row 8t + p, byte sbyte0).
+template <int NU>
+__device__ __forceinline__ void convert_units(const uint4 (&v)[NU], int nun, int t0, int blk, int j, uint32_t atom,
+                                              uint32_t img, int sbyte0) {
+    uint32_t a[NU][4], amax[NU];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) a[q] = w[q] & 0x7fff7fffu;
-    const uint32_t m = __vmaxu2(__vmaxu2(a[0], a[1]), __vmaxu2(a[2], a[3]));
-    uint32_t amax = max(m & 0xffffu, m >> 16);
-    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    for (int u = 0; u < NU; ++u) {
+        a[u][0] = v[u].x & 0x7fff7fffu;
+        a[u][1] = v[u].y & 0x7fff7fffu;
+        a[u][2] = v[u].z & 0x7fff7fffu;
+        a[u][3] = v[u].w & 0x7fff7fffu;
+        const uint32_t m = __vmaxu2(__vmaxu2(a[u][0], a[u][1]), __vmaxu2(a[u][2], a[u][3]));
+        amax[u] = max(m & 0xffffu, m >> 16);
+    }
+#pragma unroll
+    for (int u = 0; u < NU; ++u) amax[u] = max(amax[u], __shfl_xor_sync(0xffffffffu, amax[u], 1));
+#pragma unroll
+    for (int u = 0; u < NU; ++u) amax[u] = max(amax[u], __shfl_xor_sync(0xffffffffu, amax[u], 2));
     // E = floor(log2 max|x|) from the bf16 exponent field (0 for zero and
     // subnormal blocks), at least -112 so that every piece scale 2^(E - 2p)
-    // is a valid E8M0 value (byte >= 1).
-    const int e = max(static_cast<int>(amax >> 7) - 127, -112);
-    const float f = __int_as_float((142 - e) << 23);  // 2^(15 - E): exponent field in [15, 254]
-    // X = rne(|x| 2^(15-E)) < 2^16 lands in the low mantissa bits of
-    // |x| 2^(15-E) + 1.5 * 2^23 (one rounding: the product is exact).
-    const uint64_t f2 = f32x2_pack(f, f);
+    // is a valid E8M0 value (byte >= 1). X = rne(|x| 2^(15-E)) < 2^16 lands
+    // in the low mantissa bits of |x| 2^(15-E) + 1.5 * 2^23 (one rounding:
+    // the product is exact).
+    int e[NU];
+    uint32_t s[NU][8];
     const uint64_t c2 = f32x2_pack(12582912.0f, 12582912.0f);
-    uint32_t s[8];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const float2 x2 = f32x2_unpack(
-            f32x2_fma(f32x2_pack(__uint_as_float(a[q] << 16), __uint_as_float(a[q] & 0xffff0000u)), f2, c2));
-        // Digits to nibbles: bytes of X to 16-bit halves (one byte permute),
-        // then nibbles, then 2-bit fields; the sign (replicated from the
-        // bf16 sign bit by the permute's sign mode) into bit 3 of each.
-        uint32_t d0 = prmt(__float_as_uint(x2.x), 0u, 0x4140);
-        uint32_t d1 = prmt(__float_as_uint(x2.y), 0u, 0x4140);
-        d0 = (d0 | (d0 << 4)) & 0x0F0F0F0Fu;
-        d1 = (d1 | (d1 << 4)) & 0x0F0F0F0Fu;
-        d0 = (d0 | (d0 << 2)) & 0x33333333u;
-        d1 = (d1 | (d1 << 2)) & 0x33333333u;
-        s[2 * q] = d0 | (prmt(w[q], 0u, 0x9999) & 0x88888888u);
-        s[2 * q + 1] = d1 | (prmt(w[q], 0u, 0xBBBB) & 0x88888888u);
-    }
-    transpose_nibbles(s);  // s[d]: digit d of the lane's 8 elements, element i in nibble i
-    // Piece p is digit 7 - p, B row 8t + p (row % 8 == p): swizzled chunk
-    // blk ^ p, word j of the chunk.
-    const uint32_t rows = atom + static_cast<uint32_t>(t) * 1024u + 4u * static_cast<uint32_t>(j);
+    for (int u = 0; u < NU; ++u) {
+        e[u] = max(static_cast<int>(amax[u] >> 7) - 127, -112);
+        const float f = __int_as_float((142 - e[u]) << 23);  // 2^(15 - E): exponent field in [15, 254]
+        const uint64_t f2 = f32x2_pack(f, f);
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-    for (int p = 0; p < kPieces; ++p) {
-        const uint32_t ad = rows + p * 128 + ((blk ^ p) << 4);
-        asm volatile("st.shared.u32 [%0], %1;" ::"r"(ad), "r"(s[kPieces - 1 - p]) : "memory");
+        for (int q = 0; q < 4; ++q) {
+            const float2 x2 = f32x2_unpack(
+                f32x2_fma(f32x2_pack(__uint_as_float(a[u][q] << 16), __uint_as_float(a[u][q] & 0xffff0000u)), f2, c2));
+            // Digits to nibbles: bytes of X to 16-bit halves (one byte
+            // permute), then nibbles, then 2-bit fields; the sign (replicated
+            // from the bf16 sign bit by the permute's sign mode) into bit 3.
+            uint32_t d0 = prmt(__float_as_uint(x2.x), 0u, 0x4140);
+            uint32_t d1 = prmt(__float_as_uint(x2.y), 0u, 0x4140);
+            d0 = (d0 | (d0 << 4)) & 0x0F0F0F0Fu;
+            d1 = (d1 | (d1 << 4)) & 0x0F0F0F0Fu;
+            d0 = (d0 | (d0 << 2)) & 0x33333333u;
+            d1 = (d1 | (d1 << 2)) & 0x33333333u;
+            s[u][2 * q] = d0 | (prmt(w[q], 0u, 0x9999) & 0x88888888u);
+            s[u][2 * q + 1] = d1 | (prmt(w[q], 0u, 0xBBBB) & 0x88888888u);
+        }
     }
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int p = 2 * j + h;
-        const uint32_t ad = img + static_cast<uint32_t>((8 * t + p) * 16 + sbyte0);
-        asm volatile("st.shared.u8 [%0], %1;" ::"r"(ad), "r"(static_cast<uint32_t>(e - 2 * p + 127)) : "memory");
+    for (int u = 0; u < NU; ++u) transpose_nibbles(s[u]);  // s[u][d]: digit d, element i in nibble i
+#pragma unroll
+    for (int u = 0; u < NU; ++u) {
+        if (u >= nun) break;
+        const int t = t0 + 2 * u;
+        // Piece p is digit 7 - p.
+        const uint32_t base = atom + static_cast<uint32_t>(t) * 1024u + 4u * static_cast<uint32_t>(j) +
+                              (static_cast<uint32_t>(blk) << 4);
+        store_piece<0>(base, s[u][7]);
+        store_piece<1>(base, s[u][6]);
+        store_piece<2>(base, s[u][5]);
+        store_piece<3>(base, s[u][4]);
+        store_piece<4>(base, s[u][3]);
+        store_piece<5>(base, s[u][2]);
+        store_piece<6>(base, s[u][1]);
+        store_piece<7>(base, s[u][0]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int p = 2 * j + h;
+            const uint32_t ad = img + static_cast<uint32_t>((8 * t + p) * 16 + sbyte0);
+            asm volatile("st.shared.u8 [%0], %1;" ::"r"(ad), "r"(static_cast<uint32_t>(e[u] - 2 * p + 127))
+                         : "memory");
+        }
     }
 }
 
@@ -461,6 +494,7 @@ __device__ void converter(const F4Params& p, int cw, int warp, int lane, const W
     const int blk = lane >> 2, jj = lane & 3;
     const __nv_bfloat16* xl = p.x + blk * 32 + 8 * jj;
     const uint32_t lanes = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int nun = m < 2 * p.T ? (2 * p.T - m + kGroupWarps - 1) / kGroupWarps : 0;  // units of this warp
     auto load = [&](StageCursor& c, uint4 (&v)[NU]) {
         if (c.left <= 0) return;
 #pragma unroll
@@ -478,12 +512,8 @@ __device__ void converter(const F4Params& p, int cw, int warp, int lane, const W
         if (!__all_sync(0xffffffffu, mbar_wait(bars.empty_b(cur.slot), cur.phase ^ 1u, wc))) return false;
         const uint32_t bslot = b_base + cur.slot * L::kSlotB;
         const uint32_t img = img_base + cur.slot * L::kImgBytes;
-#pragma unroll
-        for (int u = 0; u < NU; ++u) {
-            const int unit = m + kGroupWarps * u;
-            if (unit < 2 * p.T)
-                convert_unit(v[u], unit >> 1, blk, jj, bslot + (unit & 1) * L::kAtomBytesB, img, 8 * (unit & 1) + blk);
-        }
+        // Units m + 4u: atom c = m & 1 for all of them, tokens m / 2 + 2u.
+        convert_units<NU>(v, nun, m >> 1, blk, jj, bslot + (m & 1) * L::kAtomBytesB, img, 8 * (m & 1) + blk);
         fence_proxy_async_shared();  // this warp's piece writes -> visible to the tensor core's reads
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.img_ready(cur.slot));

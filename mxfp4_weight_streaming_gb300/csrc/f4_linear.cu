@@ -84,40 +84,42 @@ constexpr int kMaxNA = 8;
 // Weight scales run this many (tile, stage) items ahead of their use: each
 // epilogue lane keeps a ring of 16-byte slots filled by cp.async (HBM
 // latency would otherwise stall every item).
-constexpr int kScaleAhead = 4;  // a power of two
+constexpr int kScaleAhead = 2;  // a power of two
 static_assert((kScaleAhead & (kScaleAhead - 1)) == 0, "ring index by mask");
 constexpr int kScaleRingBytes = kEpilogueWarps * kScaleAhead * 32 * 16;
 
-// Shared-memory plan (offsets from the 1024-aligned base). The activation
-// buffers first: NB buffers of 2 atoms of NPAD rows x 128 B each. Then their
-// scale images (NPAD x 16 bytes: row n's 16 block scales of the stage), the
-// mbarriers, the abort flag, the TMEM base word, the cluster inbox, the
-// epilogue warps' weight-scale rings, and last
-// the weight ring: NA slots of 2 atoms x h_main rows x 128 B, followed by
-// (128 - h_main) x 128 bytes that only the MMA's reads of a short tile's
-// missing rows touch.
+// Shared-memory plan (offsets from the 1024-aligned base). The weight ring
+// first: NA slots of 2 atoms x h_main rows x 128 B. The MMA reads 128 rows
+// of an atom whatever the tile's height, i.e. up to (128 - h_main) x 128
+// bytes past the ring's last atom; those rows' results are never read, and
+// what lies there is the next region, so no slack is needed while the
+// allocation reaches that far. Then NB activation buffers of 2 atoms of
+// NPAD rows x 128 B, their scale images (NPAD x 16 bytes: row n's 16 block
+// scales of the stage), the mbarriers, the abort flag, the TMEM base word,
+// the cluster inbox and the epilogue warps' weight-scale rings.
 template <int NPAD>
 struct Layout {
     static constexpr int kAtomBytesB = NPAD * kAtomRowBytes;
     static constexpr int kSlotB = 2 * kAtomBytesB;  // a multiple of 1024 (NPAD >= 16)
     static constexpr int kImgBytes = NPAD * 16;
-    static constexpr int kOffB = 0;
     static_assert(NPAD % 16 == 0 && NPAD >= 16 && NPAD <= 64, "MMA N");
     static_assert(kSlotB % 1024 == 0, "B buffers stay 1024-aligned for the 128-byte swizzle");
 
     // Runtime part (depends on NA, NB, the cluster inbox and h_main).
-    int off_img, off_bars, off_abort, off_tmem_slot, off_inbox, off_sc, off_a, slot_a, total;
+    int slot_a, off_b, off_img, off_bars, off_abort, off_tmem_slot, off_inbox, off_sc, total;
     __host__ __device__ Layout(int na, int nb, int inbox_bytes, int h_main) {
-        off_img = nb * kSlotB;
+        slot_a = 2 * h_main * kAtomRowBytes;  // a multiple of 2048 (h_main % 8 == 0)
+        off_b = na * slot_a;
+        off_img = off_b + nb * kSlotB;
         off_bars = off_img + nb * kImgBytes;
         const int nbars = 3 * na + 3 * nb + 4;
         off_abort = off_bars + 8 * nbars;
         off_tmem_slot = off_abort + 4;
         off_inbox = (off_tmem_slot + 4 + 127) / 128 * 128;
         off_sc = (off_inbox + inbox_bytes + 127) / 128 * 128;
-        off_a = (off_sc + kScaleRingBytes + 1023) / 1024 * 1024;
-        slot_a = 2 * h_main * kAtomRowBytes;
-        total = off_a + na * slot_a + (kTileRows - h_main) * kAtomRowBytes;
+        total = off_sc + kScaleRingBytes;
+        const int a_reach = off_b + (kTileRows - h_main) * kAtomRowBytes;
+        total = total > a_reach ? total : a_reach;
     }
 };
 
@@ -692,11 +694,13 @@ __device__ void epilogue_body(const F4Params& p, int q, int lane, const Work& w,
                     s[2 * c + h] = a;
                 }
             }
-            // Inbox row of (tile, row): the sums of tokens 4v..4v+3 in its
-            // 16-byte vector v (kInboxVec of them).
+            // Inbox row of (tile, row), rows of the tile only (every tile
+            // before the last has h_main): the sums of tokens 4v..4v+3 in
+            // its 16-byte vector v.
             constexpr int NV = inbox_vectors(NPAD);
-            const uint32_t row_off = static_cast<uint32_t>(((ti - t0) * kTileRows + rt) * NV * 16);
+            const uint32_t row_off = static_cast<uint32_t>(((ti - t0) * p.h_main + rt) * NV * 16);
             if (sender) {
+                if (rt >= tile_height(p, w, ti)) continue;
                 // Hand the fp32 sums to rank 0: asynchronous remote stores
                 // that count their bytes on rank 0's inbox barrier.
                 const uint32_t dst = map_to_rank(inbox, 0) + row_off;
@@ -708,7 +712,7 @@ __device__ void epilogue_body(const F4Params& p, int q, int lane, const Work& w,
                                 rbar);
                 continue;
             }
-            if (p.cl > 1) {
+            if (p.cl > 1 && rt < tile_height(p, w, ti)) {
 #pragma unroll
                 for (int v = 0; v < NV; ++v) {
                     const uint4 in = lds128(inbox + row_off + 16 * v);
@@ -801,9 +805,14 @@ __global__ void __launch_bounds__(kThreads, NPAD <= 32 ? 2 : 1)
         mbar_init(bars.drain(), 1);
         *abort_flag = 0;
         fence_barrier_init();
-        // Rank 0 of a cluster expects rank 1's sums of every tile, in bytes
-        // (rank 1 sends only after the cluster barrier, so this comes first).
-        if (p.cl > 1 && w.rank == 0) mbar_arrive_expect_tx(bars.inbox(), static_cast<uint32_t>(p.inbox_bytes));
+        // Rank 0 of a cluster expects rank 1's sums of every row of its
+        // tiles, in bytes (rank 1 sends only after the cluster barrier, so
+        // this comes first).
+        if (p.cl > 1 && w.rank == 0 && w.ntile > 0) {
+            int rows = 0;
+            for (int i = 0; i < w.ntile; ++i) rows += tile_height(p, w, i);
+            mbar_arrive_expect_tx(bars.inbox(), static_cast<uint32_t>(rows * inbox_vectors(NPAD) * 16));
+        }
     }
     // Rows past 8T of the B buffers (padding of the MMA's N) and their scale
     // bytes are zero for the whole kernel; the converters never write them.
@@ -814,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, NPAD <= 32 ? 2 : 1)
             uint32_t a;
             if (i < chunks) {
                 const int row = 8 * p.T + (i >> 3) % pad_rows, atom = (i >> 3) / pad_rows;  // atom over buffers
-                a = base + L::kOffB + atom * L::kAtomBytesB + (row >> 3) * 1024 + (row & 7) * 128 + (i & 7) * 16;
+                a = base + lay.off_b + atom * L::kAtomBytesB + (row >> 3) * 1024 + (row & 7) * 128 + (i & 7) * 16;
             } else {
                 const int r = i - chunks;
                 a = base + lay.off_img + (r / pad_rows) * L::kImgBytes + (8 * p.T + r % pad_rows) * 16;
@@ -834,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, NPAD <= 32 ? 2 : 1)
     // columns at the top, 16 per weight slot then 16 per activation buffer.
     const uint32_t sfa_col = static_cast<uint32_t>((p.tmem_cols - 16 * p.na - 16 * p.nb) / 32 * 32);
     const uint32_t sfb_col = sfa_col + 16u * static_cast<uint32_t>(p.na);
-    const uint32_t a_base = base + lay.off_a;
+    const uint32_t a_base = base;
 
     bool cluster_waited = false;
     if (w.ntile > 0 && w.spt > 0) {
@@ -842,9 +851,9 @@ __global__ void __launch_bounds__(kThreads, NPAD <= 32 ? 2 : 1)
             if (lane == 0) producer(p, &main_map, &tail_map, w, a_base, lay.slot_a, bars, wc);
         } else if (warp == kMmaWarp) {
             if (lane == 0)
-                mma_issuer<NPAD>(p, w, a_base, lay.slot_a, base + L::kOffB, tbase, sfa_col, sfb_col, bars, wc);
+                mma_issuer<NPAD>(p, w, a_base, lay.slot_a, base + lay.off_b, tbase, sfa_col, sfb_col, bars, wc);
         } else if (warp >= kFirstConverterWarp) {
-            converter<NPAD>(p, warp - kFirstConverterWarp, warp, lane, w, base + L::kOffB, base + lay.off_img, tbase,
+            converter<NPAD>(p, warp - kFirstConverterWarp, warp, lane, w, base + lay.off_b, base + lay.off_img, tbase,
                             sfb_col, bars, wc);
         } else {
             epilogue<NPAD>(p, warp, lane, w, base + lay.off_inbox, base + lay.off_sc, tbase, sfa_col, bars, wc,
@@ -918,7 +927,7 @@ static bool plan_fit(int npad, int cl, int t, int64_t rows, int64_t groups, int 
     const int h_main = static_cast<int>(rows < kTileRows ? rows : kTileRows);
     const int h_tail = rows > kTileRows ? static_cast<int>(rows % kTileRows) : 0;
     const int tiles = rows <= kTileRows ? 1 : static_cast<int>(rows / kTileRows) + (h_tail ? 1 : 0);
-    const int inbox = cl > 1 ? tiles * kTileRows * inbox_vectors(npad) * 16 : 0;
+    const int inbox = cl > 1 ? static_cast<int>(rows) * inbox_vectors(npad) * 16 : 0;
     const int sfa_col = (cols - 16 * na - 16 * nb) / 32 * 32;
     const int max_batch = sfa_col / npad;
     if (max_batch < 1 || (cl > 1 && max_batch < tiles)) return false;

@@ -81,6 +81,53 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking tests of two, three or four mbarrier phases in one go: the
+// tests are independent, so they cost one shared-memory round trip, not one
+// each (each is about 90 ns on GB300 with the copy engine and tensor cores
+// busy). True if every phase has completed.
+__device__ __forceinline__ bool mbar_test2(uint32_t b1, uint32_t p1, uint32_t b2, uint32_t p2) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred q1, q2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q1, [%1], %2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q2, [%3], %4;\n\t"
+        "and.pred q1, q1, q2;\n\tselp.u32 %0, 1, 0, q1;\n\t}"
+        : "=r"(ok)
+        : "r"(b1), "r"(p1), "r"(b2), "r"(p2)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ bool mbar_test3(uint32_t b1, uint32_t p1, uint32_t b2, uint32_t p2, uint32_t b3,
+                                           uint32_t p3) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred q1, q2, q3;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q1, [%1], %2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q2, [%3], %4;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q3, [%5], %6;\n\t"
+        "and.pred q1, q1, q2;\n\tand.pred q1, q1, q3;\n\tselp.u32 %0, 1, 0, q1;\n\t}"
+        : "=r"(ok)
+        : "r"(b1), "r"(p1), "r"(b2), "r"(p2), "r"(b3), "r"(p3)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_test4(uint32_t b1, uint32_t p1, uint32_t b2, uint32_t p2, uint32_t b3,
+                                           uint32_t p3, uint32_t b4, uint32_t p4) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred q1, q2, q3, q4;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q1, [%1], %2;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q2, [%3], %4;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q3, [%5], %6;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 q4, [%7], %8;\n\t"
+        "and.pred q1, q1, q2;\n\tand.pred q3, q3, q4;\n\tand.pred q1, q1, q3;\n\tselp.u32 %0, 1, 0, q1;\n\t}"
+        : "=r"(ok)
+        : "r"(b1), "r"(p1), "r"(b2), "r"(p2), "r"(b3), "r"(p3), "r"(b4), "r"(p4)
+        : "memory");
+    return ok != 0;
+}
+
 // Where a bounded wait reports: the per-device status word, and a per-CTA
 // abort flag in shared memory. Once one wait of a CTA has given up, every
 // later wait of that CTA fails at once, so the CTA winds down in one limit

@@ -174,37 +174,6 @@ __device__ __forceinline__ void cluster_arrive() {
 }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
-// Non-blocking tests of two or three mbarrier phases in one go: the tests
-// are independent, so they cost one shared-memory round trip, not one each
-// (each is about 90 ns on GB300 with the copy engine and tensor cores
-// busy). True if every phase has completed.
-__device__ __forceinline__ bool mbar_test2(uint32_t b1, uint32_t p1, uint32_t b2, uint32_t p2) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred q1, q2;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 q1, [%1], %2;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 q2, [%3], %4;\n\t"
-        "and.pred q1, q1, q2;\n\tselp.u32 %0, 1, 0, q1;\n\t}"
-        : "=r"(ok)
-        : "r"(b1), "r"(p1), "r"(b2), "r"(p2)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ bool mbar_test3(uint32_t b1, uint32_t p1, uint32_t b2, uint32_t p2, uint32_t b3,
-                                           uint32_t p3) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred q1, q2, q3;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 q1, [%1], %2;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 q2, [%3], %4;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 q3, [%5], %6;\n\t"
-        "and.pred q1, q1, q2;\n\tand.pred q1, q1, q3;\n\tselp.u32 %0, 1, 0, q1;\n\t}"
-        : "=r"(ok)
-        : "r"(b1), "r"(p1), "r"(b2), "r"(p2), "r"(b3), "r"(p3)
-        : "memory");
-    return ok != 0;
-}
-
 // ------------------------------------------------------------- producer
 __device__ void producer(const F4Params& p, const CUtensorMap* main_map, const CUtensorMap* tail_map, const Work& w,
                          uint32_t a_base, int slot_a, const Bars& bars, const WaitCtx& wc) {

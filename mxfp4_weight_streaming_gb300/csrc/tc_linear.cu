@@ -211,16 +211,25 @@ __device__ bool mma_issue_all(const Work& w, uint32_t base, uint32_t tbase, cons
         if (!mbar_wait(bars.acc_empty(), (static_cast<uint32_t>(b) & 1u) ^ 1u, wc)) return false;
         for (int k = 0; k < w.spt; ++k) {
             const int off = ((w.st0 + k) * SA) & 3;  // the stage's first atom within its 4-atom scale group
-            if (!mbar_wait(bars.full_b(rb.slot), rb.phase, wc)) return false;
-            if (!mbar_wait(bars.sfb_ready(rb.slot), rb.phase, wc)) return false;
             uint64_t bd = 0;
 #pragma unroll
             for (int s = 0; s < NG; ++s)
                 if (s == rb.slot) bd = bdesc[s];
             const uint32_t sfb = tbase + C::kSfbCol + rb.slot * 16;
             for (int ti = 0; ti < bt; ++ti) {
-                if (!mbar_wait(bars.full_a(ra.slot), ra.phase, wc)) return false;
-                if (!mbar_wait(bars.sfa_ready(ra.slot), ra.phase, wc)) return false;
+                // The stage's activations and their scales (first tile only),
+                // the tile's weights and its scales: all tested at once, and
+                // waited for one by one (bounded) only if some are not there.
+                const bool ready =
+                    ti == 0 ? mbar_test4(bars.full_b(rb.slot), rb.phase, bars.sfb_ready(rb.slot), rb.phase,
+                                         bars.full_a(ra.slot), ra.phase, bars.sfa_ready(ra.slot), ra.phase)
+                            : mbar_test2(bars.full_a(ra.slot), ra.phase, bars.sfa_ready(ra.slot), ra.phase);
+                if (!ready) {
+                    if (ti == 0 && !mbar_wait(bars.full_b(rb.slot), rb.phase, wc)) return false;
+                    if (ti == 0 && !mbar_wait(bars.sfb_ready(rb.slot), rb.phase, wc)) return false;
+                    if (!mbar_wait(bars.full_a(ra.slot), ra.phase, wc)) return false;
+                    if (!mbar_wait(bars.sfa_ready(ra.slot), ra.phase, wc)) return false;
+                }
                 fence_after_sync();
                 uint64_t ad = 0;
 #pragma unroll

@@ -483,8 +483,15 @@ __device__ void converter(const F4Params& p, int cw, int warp, int lane, const W
         if (!__all_sync(0xffffffffu, mbar_wait(bars.empty_b(cur.slot), cur.phase ^ 1u, wc))) return false;
         const uint32_t bslot = b_base + cur.slot * L::kSlotB;
         const uint32_t img = img_base + cur.slot * L::kImgBytes;
-        // Units m + 4u: atom c = m & 1 for all of them, tokens m / 2 + 2u.
-        convert_units<NU>(v, nun, m >> 1, blk, jj, bslot + (m & 1) * L::kAtomBytesB, img, 8 * (m & 1) + blk);
+        // Units m + 4u: atom c = m & 1 for all of them, tokens m / 2 + 2u;
+        // one after the other (in isolation two units in lockstep measured
+        // 676 cycles against 2 x 290 one at a time).
+#pragma unroll
+        for (int u = 0; u < NU; ++u) {
+            if (u >= nun) break;
+            const uint4 vu[1] = {v[u]};
+            convert_units<1>(vu, 1, (m >> 1) + 2 * u, blk, jj, bslot + (m & 1) * L::kAtomBytesB, img, 8 * (m & 1) + blk);
+        }
         fence_proxy_async_shared();  // this warp's piece writes -> visible to the tensor core's reads
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.img_ready(cur.slot));

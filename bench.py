@@ -459,8 +459,10 @@ def ffn_chain_bytes(t: int, hidden: int, inter: int) -> int:
 
 
 def measure_ffn_chain(wl_name: str, device, clocks, calls_target: int = 1200, replays: int = 12):
-    """Fused dense FFN chain (one mxfp4_ffn call = one cooperative launch
-    plus a 4-byte memset): per-call time and GB/s of W1 + W2 (+ x, y)."""
+    """Dense FFN chain (one mxfp4_ffn call: for t <= 4 with hidden and inter
+    multiples of 512, two packed-E2M1 launches chained by programmatic
+    dependent launch; otherwise one cooperative launch plus a 4-byte
+    memset): per-call time and GB/s of W1 + W2 (+ x, y)."""
     import torch
 
     import mxfp4_weight_streaming_gb300 as mx
@@ -499,10 +501,14 @@ def measure_ffn_chain(wl_name: str, device, clocks, calls_target: int = 1200, re
     nbytes = ffn_chain_bytes(t, hidden, inter)
     peak, _ = hbm_peak()
     gbs = nbytes / (us * 1e-6) / 1e9
+    two_launch = t <= 4 and hidden % 512 == 0 and inter % 512 == 0
+    kernel = ("mxfp4::f4::f4_linear_kernel<npad, 0> (W1, fp32 a|b) then f4_linear_kernel<npad, 1> "
+              "(W2, SiLU(a)*b converted in the kernel)" if two_launch else
+              "mxfp4::ffn_chain_kernel (stream_body<FfnUp> then stream_body<FfnDown>, cooperative)")
     return {"us_per_call": round(us, 3), "GBps": round(gbs, 1), "frac": round(gbs / peak, 4),
             "spread_us_per_call": percentiles(per_call), "calls": calls, "bytes_per_call": nbytes,
-            "kernel": "mxfp4::ffn_chain_kernel (stream_body<FfnUp> then stream_body<FfnDown>, cooperative)",
-            "launches_per_call": 1, "memsets_per_call": 1,
+            "kernel": kernel, "launches_per_call": 2 if two_launch else 1,
+            "memsets_per_call": 0 if two_launch else 1,
             "clocks": clocks.summary(wall0 - 0.5, wall1 + 0.1)}
 
 

@@ -245,14 +245,23 @@ int mxfp4_moe_shared(const void* x, int64_t t, int64_t hidden, const float* rout
 size_t mxfp4_ffn_workspace_size(int64_t t, int64_t hidden, int64_t inter);
 
 /*
- * Fused dense FFN chain, up -> SwiGLU -> down, in ONE persistent kernel
- * launch (lithosai "Low-Latency Inference on AMD MI355X" and AMD
- * "megakernel-intro", section "1. Megakernels": a layer's stages in one
- * kernel, SMs that finish a stage early preloading the next stage's
- * weights). The arithmetic is one SwiGLU expert of mxfp4_moe applied to
- * every token with weight 1. For each token t:
+ * Dense FFN chain, up -> SwiGLU -> down (lithosai "Low-Latency Inference on
+ * AMD MI355X" and AMD "megakernel-intro", section "1. Megakernels": a
+ * layer's stages back to back, the next stage's weights preloaded while the
+ * previous one runs). The arithmetic is one SwiGLU expert of mxfp4_moe
+ * applied to every token with weight 1. For each token t:
  *   a = W1[0:inter] x_t (gate rows), b = W1[inter:2*inter] x_t (up rows),
- *   h = SiLU(a) * b (fp32, in the workspace), y[t] = bf16( W2 h ).
+ *   h = SiLU(a) * b (fp32), y[t] = bf16( W2 h ).
+ * Two forms, chosen by shape:
+ *   t <= 4 with hidden and inter multiples of 512: two launches of the
+ *     packed-E2M1 tensor-core kernel on the stream. The first writes a | b
+ *     in fp32 to the workspace; the second computes h = SiLU(a) * b in fp32
+ *     while it converts its activations (digit pieces of h: each element
+ *     within 2^(E-16) of its value, E its 32-block's largest exponent), and
+ *     starts streaming W2 before the first has finished (programmatic
+ *     dependent launch: it waits only where it reads a | b).
+ *   otherwise: ONE persistent cooperative launch (h in the workspace),
+ *     preceded by a 4-byte memset of the workspace.
  *   x              device bf16 [t, hidden], 16-byte aligned; 1 <= t <= 8
  *   hidden, inter  multiples of 32, at most 2^20 (MXFP4_ERR_SHAPE also when
  *                  the staged activations of one phase do not fit on chip)
@@ -263,11 +272,10 @@ size_t mxfp4_ffn_workspace_size(int64_t t, int64_t hidden, int64_t inter);
  *   y              device bf16 [t, hidden] (output)
  *   workspace      device scratch of at least mxfp4_ffn_workspace_size()
  *                  bytes, 256-byte aligned; contents on entry do not matter.
- * The kernel is a cooperative launch: every CTA waits (bounded) for the
- * gate/up results of all the others, so the whole grid must be resident. A
- * call that shares the GPU with other work that holds SMs may therefore end
- * in MXFP4_ERR_TIMEOUT (reported as for every call) instead of a result.
- * The call enqueues a 4-byte memset of the workspace before the kernel.
+ * The cooperative form's CTAs wait (bounded) for the gate/up results of all
+ * the others, so the whole grid must be resident. A call that shares the
+ * GPU with other work that holds SMs may therefore end in MXFP4_ERR_TIMEOUT
+ * (reported as for every call) instead of a result.
  */
 int mxfp4_ffn(const void* x, int64_t t, int64_t hidden, const uint8_t* w1q, const uint8_t* w1s, const uint8_t* w2q,
               const uint8_t* w2s, int64_t inter, void* y, void* workspace, size_t workspace_bytes, void* stream);

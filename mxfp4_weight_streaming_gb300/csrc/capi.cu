@@ -227,6 +227,76 @@ int linear_shape_status(int64_t t, int64_t k, int64_t n) {
     return MXFP4_OK;
 }
 
+// Kernel arguments of one packed-E2M1 call with plan fp (inputs and outputs
+// set by the caller).
+mxfp4::f4::F4Params f4_params(const mxfp4::f4::F4Plan& fp, const uint8_t* ws, unsigned* status, int64_t t,
+                              int64_t k, int64_t n) {
+    mxfp4::f4::F4Params q{};
+    q.ws = ws;
+    q.status = status;
+    q.T = static_cast<int>(t);
+    q.K = static_cast<int>(k);
+    q.N = static_cast<int>(n);
+    q.nblk = static_cast<int>(k / 32);
+    q.stages = static_cast<int>(k / 512);
+    q.rows = fp.rows;
+    q.h_main = fp.h_main;
+    q.h_tail = fp.h_tail;
+    q.cl = fp.cl;
+    q.na = fp.na;
+    q.nb = fp.nb;
+    q.max_batch = fp.max_batch;
+    q.tmem_cols = fp.tmem_cols;
+    q.inbox_bytes = fp.inbox_bytes;
+    return q;
+}
+
+// The FFN chain on the packed-E2M1 kernel: W1 [2 inter, hidden] with fp32
+// outputs a | b into the workspace, then W2 [hidden, inter] whose
+// conversion takes SiLU(a) * b. Plans and tensor maps per weight set.
+struct FfnF4Plan {
+    int dev = -1;
+    const uint8_t* w1q = nullptr;
+    const uint8_t* w2q = nullptr;
+    int64_t t = 0, hidden = 0, inter = 0;
+    mxfp4::f4::F4Plan up{}, down{};
+    CUtensorMap up_map, up_tail, down_map, down_tail;
+};
+thread_local FfnF4Plan t_ffn_plans[4];
+thread_local int t_ffn_next = 0;
+
+// The plan of an FFN call on the packed-E2M1 kernel, or null when the shape
+// is outside it (t > 4, hidden or inter not a multiple of 512, no fit).
+const FfnF4Plan* ffn_f4_plan(int dev, const DeviceInfo* d, const uint8_t* w1q, const uint8_t* w2q, int64_t t,
+                             int64_t hidden, int64_t inter, int* rc) {
+    *rc = MXFP4_OK;
+    for (const FfnF4Plan& c : t_ffn_plans)
+        if (c.dev == dev && c.w1q == w1q && c.w2q == w2q && c.t == t && c.hidden == hidden && c.inter == inter)
+            return &c;
+    if (t > 4 || hidden % 512 != 0 || inter % 512 != 0) return nullptr;
+    FfnF4Plan f;
+    if (!mxfp4::f4::plan_f4(static_cast<int>(t), hidden, 2 * inter, d->num_sms, d->max_smem, &f.up) ||
+        !mxfp4::f4::plan_f4(static_cast<int>(t), inter, hidden, d->num_sms, d->max_smem, &f.down, true))
+        return nullptr;
+    if ((*rc = encode_f4_weight_map(&f.up_map, w1q, 2 * inter, hidden, f.up.h_main))) return nullptr;
+    f.up_tail = f.up_map;
+    if (f.up.h_tail && (*rc = encode_f4_weight_map(&f.up_tail, w1q, 2 * inter, hidden, f.up.h_tail))) return nullptr;
+    if ((*rc = encode_f4_weight_map(&f.down_map, w2q, hidden, inter, f.down.h_main))) return nullptr;
+    f.down_tail = f.down_map;
+    if (f.down.h_tail && (*rc = encode_f4_weight_map(&f.down_tail, w2q, hidden, inter, f.down.h_tail)))
+        return nullptr;
+    f.dev = dev;
+    f.w1q = w1q;
+    f.w2q = w2q;
+    f.t = t;
+    f.hidden = hidden;
+    f.inter = inter;
+    FfnF4Plan* slot = &t_ffn_plans[t_ffn_next];
+    t_ffn_next = (t_ffn_next + 1) % 4;
+    *slot = f;
+    return slot;
+}
+
 }  // namespace
 
 extern "C" {
@@ -303,25 +373,9 @@ int mxfp4_linear(const void* x, int64_t t, int64_t k, const uint8_t* wq, const u
     const CUtensorMap& map = plan->map;
     if (plan->kind == 2) {
         const mxfp4::f4::F4Plan& fp = plan->fp;
-        mxfp4::f4::F4Params q{};
+        mxfp4::f4::F4Params q = f4_params(fp, ws, d->status, t, k, n);
         q.x = static_cast<const __nv_bfloat16*>(x);
-        q.ws = ws;
         q.y = static_cast<__nv_bfloat16*>(y);
-        q.status = d->status;
-        q.T = static_cast<int>(t);
-        q.K = static_cast<int>(k);
-        q.N = static_cast<int>(n);
-        q.nblk = static_cast<int>(k / 32);
-        q.stages = static_cast<int>(k / 512);
-        q.rows = fp.rows;
-        q.h_main = fp.h_main;
-        q.h_tail = fp.h_tail;
-        q.cl = fp.cl;
-        q.na = fp.na;
-        q.nb = fp.nb;
-        q.max_batch = fp.max_batch;
-        q.tmem_cols = fp.tmem_cols;
-        q.inbox_bytes = fp.inbox_bytes;
         cudaError_t e = mxfp4::f4::launch_f4_linear(map, plan->tail_map, q, fp, static_cast<cudaStream_t>(stream));
         return e == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
     }
@@ -508,6 +562,25 @@ int mxfp4_ffn(const void* x, int64_t t, int64_t hidden, const uint8_t* w1q, cons
     if (workspace_bytes < mxfp4::ffn_workspace_bytes(t, inter)) return MXFP4_ERR_WORKSPACE;
     DeviceInfo* d = nullptr;
     if (int rc = device_info(&d)) return rc;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int prc = MXFP4_OK;
+    if (const FfnF4Plan* f = ffn_f4_plan(dev, d, w1q, w2q, t, hidden, inter, &prc)) {
+        // Two launches on the stream, the second waiting for the first only
+        // where it reads a | b (programmatic dependent launch).
+        float* ab = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + 256);
+        mxfp4::f4::F4Params q1 = f4_params(f->up, w1s, d->status, t, hidden, 2 * inter);
+        q1.x = static_cast<const __nv_bfloat16*>(x);
+        q1.yf = ab;
+        cudaError_t e = mxfp4::f4::launch_f4_linear(f->up_map, f->up_tail, q1, f->up, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return MXFP4_ERR_CUDA;
+        mxfp4::f4::F4Params q2 = f4_params(f->down, w2s, d->status, t, inter, hidden);
+        q2.xab = ab;
+        q2.y = static_cast<__nv_bfloat16*>(y);
+        e = mxfp4::f4::launch_f4_linear(f->down_map, f->down_tail, q2, f->down, static_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
+    }
+    if (prc != MXFP4_OK) return prc;
     mxfp4::FfnPlan plan{};
     if (int rc = mxfp4::plan_ffn(static_cast<int>(t), static_cast<int>(hidden), static_cast<int>(inter), d->max_smem,
                                  &plan))

@@ -329,87 +329,109 @@ __device__ __forceinline__ void store_piece(uint32_t base, uint32_t v) {
     asm volatile("st.shared.u32 [%0+%2], %1;" ::"r"(base ^ (P << 4)), "r"(v), "n"(P * 128) : "memory");
 }
 
-// The units of one converter warp in one stage, converted in lockstep (each
-// step for all of them before the next, so their dependent chains overlap).
-// Unit u holds one lane's 8 consecutive activations of a 32-value block (one
-// 16-byte load; word q holds elements 2q (low half) and 2q + 1) of token
-// t0 + 2u; the block is held by the 4 lanes l with l >> 2 == blk (j = l & 3
-// holds elements 8j..8j+7). Units u < nun are written: the lane's word of
-// each of the token's 8 piece rows of the swizzled B atom, and the scale
-// bytes of pieces 2j and 2j + 1 (image row 8t + p, byte sbyte0).
-template <int NU>
-__device__ __forceinline__ void convert_units(const uint4 (&v)[NU], int nun, int t0, int blk, int j, uint32_t atom,
-                                              uint32_t img, int sbyte0) {
-    uint32_t a[NU][4], amax[NU];
+// One element pair's digit words: X of elements 2q and 2q + 1 in the low
+// 16 bits of x2.x and x2.y; sg0 / sg1 hold each element's sign bit copied
+// into bit 7 of every byte. Word i gets element i's eight 2-bit digits,
+// digit d in bits 4d and 4d + 1, the sign in bit 4d + 3: the bytes of X go
+// to 16-bit halves (one byte permute), then to nibbles, then to 2-bit
+// fields.
+__device__ __forceinline__ void digit_words(float2 x2, uint32_t sg0, uint32_t sg1, uint32_t& w0, uint32_t& w1) {
+    uint32_t d0 = prmt(__float_as_uint(x2.x), 0u, 0x4140);
+    uint32_t d1 = prmt(__float_as_uint(x2.y), 0u, 0x4140);
+    d0 = (d0 | (d0 << 4)) & 0x0F0F0F0Fu;
+    d1 = (d1 | (d1 << 4)) & 0x0F0F0F0Fu;
+    d0 = (d0 | (d0 << 2)) & 0x33333333u;
+    d1 = (d1 | (d1 << 2)) & 0x33333333u;
+    w0 = d0 | (sg0 & 0x88888888u);
+    w1 = d1 | (sg1 & 0x88888888u);
+}
+
+// Writes one unit (token t): after the transpose, the lane's word of each of
+// the token's 8 piece rows of the swizzled B atom (piece p is digit 7 - p),
+// and the scale bytes E - 2p + 127 of pieces 2j and 2j + 1 (image row
+// 8t + p, byte sbyte0).
+__device__ __forceinline__ void emit_unit(uint32_t (&s)[8], int e, int t, int blk, int j, uint32_t atom,
+                                          uint32_t img, int sbyte0) {
+    transpose_nibbles(s);  // s[d]: digit d, element i in nibble i
+    const uint32_t base = atom + static_cast<uint32_t>(t) * 1024u + 4u * static_cast<uint32_t>(j) +
+                          (static_cast<uint32_t>(blk) << 4);
+    store_piece<0>(base, s[7]);
+    store_piece<1>(base, s[6]);
+    store_piece<2>(base, s[5]);
+    store_piece<3>(base, s[4]);
+    store_piece<4>(base, s[3]);
+    store_piece<5>(base, s[2]);
+    store_piece<6>(base, s[1]);
+    store_piece<7>(base, s[0]);
 #pragma unroll
-    for (int u = 0; u < NU; ++u) {
-        a[u][0] = v[u].x & 0x7fff7fffu;
-        a[u][1] = v[u].y & 0x7fff7fffu;
-        a[u][2] = v[u].z & 0x7fff7fffu;
-        a[u][3] = v[u].w & 0x7fff7fffu;
-        const uint32_t m = __vmaxu2(__vmaxu2(a[u][0], a[u][1]), __vmaxu2(a[u][2], a[u][3]));
-        amax[u] = max(m & 0xffffu, m >> 16);
+    for (int h = 0; h < 2; ++h) {
+        const int p = 2 * j + h;
+        const uint32_t ad = img + static_cast<uint32_t>((8 * t + p) * 16 + sbyte0);
+        asm volatile("st.shared.u8 [%0], %1;" ::"r"(ad), "r"(static_cast<uint32_t>(e - 2 * p + 127)) : "memory");
     }
+}
+
+// The block exponent E from the largest magnitude's exponent field (0 for
+// zero and subnormal blocks), at least -112 so that every piece scale
+// 2^(E - 2p) is a valid E8M0 value (byte >= 1); returned with the factor
+// 2^(15 - E) (exponent field in [14, 254]). X = rne(|x| 2^(15-E)) < 2^16
+// then lands in the low mantissa bits of |x| 2^(15-E) + 1.5 * 2^23 (one
+// rounding: the product is exact).
+__device__ __forceinline__ int block_exponent(int field, float& f) {
+    const int e = max(field - 127, -112);
+    f = __int_as_float((142 - e) << 23);
+    return e;
+}
+
+// One unit of bf16 activations: a lane's 8 consecutive values of a 32-value
+// block (one 16-byte load; word q holds elements 2q (low half) and 2q + 1),
+// token t; the block is held by the 4 lanes l with l >> 2 == blk (j = l & 3
+// holds elements 8j..8j+7).
+__device__ __forceinline__ void convert_unit(const uint4& v, int t, int blk, int j, uint32_t atom, uint32_t img,
+                                             int sbyte0) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t a[4];
 #pragma unroll
-    for (int u = 0; u < NU; ++u) amax[u] = max(amax[u], __shfl_xor_sync(0xffffffffu, amax[u], 1));
+    for (int q = 0; q < 4; ++q) a[q] = w[q] & 0x7fff7fffu;
+    const uint32_t m = __vmaxu2(__vmaxu2(a[0], a[1]), __vmaxu2(a[2], a[3]));
+    uint32_t amax = max(m & 0xffffu, m >> 16);
+    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    float f;
+    const int e = block_exponent(static_cast<int>(amax >> 7), f);
+    const uint64_t f2 = f32x2_pack(f, f), c2 = f32x2_pack(12582912.0f, 12582912.0f);
+    uint32_t s[8];
 #pragma unroll
-    for (int u = 0; u < NU; ++u) amax[u] = max(amax[u], __shfl_xor_sync(0xffffffffu, amax[u], 2));
-    // E = floor(log2 max|x|) from the bf16 exponent field (0 for zero and
-    // subnormal blocks), at least -112 so that every piece scale 2^(E - 2p)
-    // is a valid E8M0 value (byte >= 1). X = rne(|x| 2^(15-E)) < 2^16 lands
-    // in the low mantissa bits of |x| 2^(15-E) + 1.5 * 2^23 (one rounding:
-    // the product is exact).
-    int e[NU];
-    uint32_t s[NU][8];
-    const uint64_t c2 = f32x2_pack(12582912.0f, 12582912.0f);
-#pragma unroll
-    for (int u = 0; u < NU; ++u) {
-        e[u] = max(static_cast<int>(amax[u] >> 7) - 127, -112);
-        const float f = __int_as_float((142 - e[u]) << 23);  // 2^(15 - E): exponent field in [15, 254]
-        const uint64_t f2 = f32x2_pack(f, f);
-        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float2 x2 = f32x2_unpack(
-                f32x2_fma(f32x2_pack(__uint_as_float(a[u][q] << 16), __uint_as_float(a[u][q] & 0xffff0000u)), f2, c2));
-            // Digits to nibbles: bytes of X to 16-bit halves (one byte
-            // permute), then nibbles, then 2-bit fields; the sign (replicated
-            // from the bf16 sign bit by the permute's sign mode) into bit 3.
-            uint32_t d0 = prmt(__float_as_uint(x2.x), 0u, 0x4140);
-            uint32_t d1 = prmt(__float_as_uint(x2.y), 0u, 0x4140);
-            d0 = (d0 | (d0 << 4)) & 0x0F0F0F0Fu;
-            d1 = (d1 | (d1 << 4)) & 0x0F0F0F0Fu;
-            d0 = (d0 | (d0 << 2)) & 0x33333333u;
-            d1 = (d1 | (d1 << 2)) & 0x33333333u;
-            s[u][2 * q] = d0 | (prmt(w[q], 0u, 0x9999) & 0x88888888u);
-            s[u][2 * q + 1] = d1 | (prmt(w[q], 0u, 0xBBBB) & 0x88888888u);
-        }
+    for (int q = 0; q < 4; ++q) {
+        const float2 x2 = f32x2_unpack(
+            f32x2_fma(f32x2_pack(__uint_as_float(a[q] << 16), __uint_as_float(a[q] & 0xffff0000u)), f2, c2));
+        // The permute's sign mode copies bit 15 (byte 1) or bit 31 (byte 3).
+        digit_words(x2, prmt(w[q], 0u, 0x9999), prmt(w[q], 0u, 0xBBBB), s[2 * q], s[2 * q + 1]);
     }
+    emit_unit(s, e, t, blk, j, atom, img, sbyte0);
+}
+
+// The same for 8 fp32 values (elements 0..7 of the lane's share).
+__device__ __forceinline__ void convert_unit_f32(const float (&h)[8], int t, int blk, int j, uint32_t atom,
+                                                 uint32_t img, int sbyte0) {
+    uint32_t a[8];
 #pragma unroll
-    for (int u = 0; u < NU; ++u) transpose_nibbles(s[u]);  // s[u][d]: digit d, element i in nibble i
+    for (int i = 0; i < 8; ++i) a[i] = __float_as_uint(h[i]) & 0x7fffffffu;
+    uint32_t amax = max(max(max(a[0], a[1]), max(a[2], a[3])), max(max(a[4], a[5]), max(a[6], a[7])));
+    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    float f;
+    const int e = block_exponent(static_cast<int>(amax >> 23), f);
+    const uint64_t f2 = f32x2_pack(f, f), c2 = f32x2_pack(12582912.0f, 12582912.0f);
+    uint32_t s[8];
 #pragma unroll
-    for (int u = 0; u < NU; ++u) {
-        if (u >= nun) break;
-        const int t = t0 + 2 * u;
-        // Piece p is digit 7 - p.
-        const uint32_t base = atom + static_cast<uint32_t>(t) * 1024u + 4u * static_cast<uint32_t>(j) +
-                              (static_cast<uint32_t>(blk) << 4);
-        store_piece<0>(base, s[u][7]);
-        store_piece<1>(base, s[u][6]);
-        store_piece<2>(base, s[u][5]);
-        store_piece<3>(base, s[u][4]);
-        store_piece<4>(base, s[u][3]);
-        store_piece<5>(base, s[u][2]);
-        store_piece<6>(base, s[u][1]);
-        store_piece<7>(base, s[u][0]);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int p = 2 * j + h;
-            const uint32_t ad = img + static_cast<uint32_t>((8 * t + p) * 16 + sbyte0);
-            asm volatile("st.shared.u8 [%0], %1;" ::"r"(ad), "r"(static_cast<uint32_t>(e[u] - 2 * p + 127))
-                         : "memory");
-        }
+    for (int q = 0; q < 4; ++q) {
+        const float2 x2 =
+            f32x2_unpack(f32x2_fma(f32x2_pack(__uint_as_float(a[2 * q]), __uint_as_float(a[2 * q + 1])), f2, c2));
+        digit_words(x2, prmt(__float_as_uint(h[2 * q]), 0u, 0xBBBB), prmt(__float_as_uint(h[2 * q + 1]), 0u, 0xBBBB),
+                    s[2 * q], s[2 * q + 1]);
     }
+    emit_unit(s, e, t, blk, j, atom, img, sbyte0);
 }
 
 // Converter groups. Group g converts stages g, g + kGroups, ...; warp m of
@@ -449,11 +471,15 @@ __device__ __forceinline__ void store_b_scale_words(uint32_t taddr, const uint4&
     fence_before_sync();
 }
 
-template <int NPAD>
+// IN = 0: x is bf16 [T, K]. IN = 1: x[t, k] = SiLU(a) * b in fp32 with
+// a = xab[t, k] and b = xab[t, K + k] (rows of 2K floats), a 32-byte load
+// of each per unit and 8 fp32 values converted.
+template <int NPAD, int IN>
 __device__ void converter(const F4Params& p, int cw, int warp, int lane, const Work& w, uint32_t b_base,
                           uint32_t img_base, uint32_t tbase, uint32_t sfb_col, const Bars& bars, const WaitCtx& wc) {
     using L = Layout<NPAD>;
     constexpr int NU = NPAD / 16;
+    constexpr int NW = IN ? 4 : 1;  // 16-byte loads per unit
     const int g = cw / kGroupWarps, m = cw % kGroupWarps;
     const int nst = w.nbatch * w.spt;
     const int nstg = nst > g ? (nst - g + kGroups - 1) / kGroups : 0;
@@ -463,23 +489,32 @@ __device__ void converter(const F4Params& p, int cw, int warp, int lane, const W
     StageCursor cur{nstg, w.st0 + g % w.spt, g % nb, static_cast<uint32_t>((g / nb) & 1)};
     StageCursor ld = cur;
     const int blk = lane >> 2, jj = lane & 3;
-    const __nv_bfloat16* xl = p.x + blk * 32 + 8 * jj;
+    const __nv_bfloat16* xl = IN == 0 ? p.x + blk * 32 + 8 * jj : nullptr;
+    const float* xf = IN == 1 ? p.xab + blk * 32 + 8 * jj : nullptr;
     const uint32_t lanes = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int nun = m < 2 * p.T ? (2 * p.T - m + kGroupWarps - 1) / kGroupWarps : 0;  // units of this warp
-    auto load = [&](StageCursor& c, uint4 (&v)[NU]) {
+    auto load = [&](StageCursor& c, uint4 (&v)[NU][NW]) {
         if (c.left <= 0) return;
 #pragma unroll
         for (int u = 0; u < NU; ++u) {
             const int unit = m + kGroupWarps * u;
             // Through L2 only: x may have been written by the previous kernel
             // of the stream, which this kernel overlaps.
-            if (unit < 2 * p.T)
-                v[u] = __ldcg(reinterpret_cast<const uint4*>(xl + static_cast<size_t>(unit >> 1) * p.K +
-                                                             static_cast<size_t>(c.k) * kStageK + (unit & 1) * 256));
+            if (unit >= 2 * p.T) continue;
+            const size_t off = static_cast<size_t>(c.k) * kStageK + (unit & 1) * 256;
+            if (IN == 0) {
+                v[u][0] = __ldcg(reinterpret_cast<const uint4*>(xl + static_cast<size_t>(unit >> 1) * p.K + off));
+            } else {
+                const float* a = xf + static_cast<size_t>(unit >> 1) * 2 * p.K + off;
+                v[u][0] = __ldcg(reinterpret_cast<const uint4*>(a));
+                v[u][NW > 1 ? 1 : 0] = __ldcg(reinterpret_cast<const uint4*>(a + 4));
+                v[u][NW > 2 ? 2 : 0] = __ldcg(reinterpret_cast<const uint4*>(a + p.K));
+                v[u][NW > 3 ? 3 : 0] = __ldcg(reinterpret_cast<const uint4*>(a + p.K + 4));
+            }
         }
         c.next(w.st0, w.spt, nb);
     };
-    auto stage = [&](const uint4 (&v)[NU]) -> bool {
+    auto stage = [&](const uint4 (&v)[NU][NW]) -> bool {
         if (!__all_sync(0xffffffffu, mbar_wait(bars.empty_b(cur.slot), cur.phase ^ 1u, wc))) return false;
         const uint32_t bslot = b_base + cur.slot * L::kSlotB;
         const uint32_t img = img_base + cur.slot * L::kImgBytes;
@@ -489,8 +524,22 @@ __device__ void converter(const F4Params& p, int cw, int warp, int lane, const W
 #pragma unroll
         for (int u = 0; u < NU; ++u) {
             if (u >= nun) break;
-            const uint4 vu[1] = {v[u]};
-            convert_units<1>(vu, 1, (m >> 1) + 2 * u, blk, jj, bslot + (m & 1) * L::kAtomBytesB, img, 8 * (m & 1) + blk);
+            const uint32_t atom = bslot + (m & 1) * L::kAtomBytesB;
+            if (IN == 0) {
+                convert_unit(v[u][0], (m >> 1) + 2 * u, blk, jj, atom, img, 8 * (m & 1) + blk);
+            } else {
+                const uint4 a0 = v[u][0], a1 = v[u][NW > 1 ? 1 : 0], b0 = v[u][NW > 2 ? 2 : 0],
+                            b1 = v[u][NW > 3 ? 3 : 0];
+                const uint32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                const uint32_t bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                float h[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float a = __uint_as_float(av[i]);
+                    h[i] = a / (1.0f + expf(-a)) * __uint_as_float(bv[i]);  // SiLU(a) * b
+                }
+                convert_unit_f32(h, (m >> 1) + 2 * u, blk, jj, atom, img, 8 * (m & 1) + blk);
+            }
         }
         fence_proxy_async_shared();  // this warp's piece writes -> visible to the tensor core's reads
         __syncwarp();
@@ -504,7 +553,7 @@ __device__ void converter(const F4Params& p, int cw, int warp, int lane, const W
         cur.next(w.st0, w.spt, nb);
         return true;
     };
-    uint4 va[NU], vb[NU];
+    uint4 va[NU][NW], vb[NU][NW];
     load(ld, va);
     load(ld, vb);
     while (cur.left > 0) {
@@ -702,8 +751,14 @@ __device__ void epilogue_body(const F4Params& p, int q, int lane, const Work& w,
             const int row = w.tile_row0(ti) + rt;
             if (rt < tile_height(p, w, ti) && row < p.N) {
 #pragma unroll
-                for (int t = 0; t < NPAD / 8; ++t)
-                    if (t < T) p.y[static_cast<size_t>(t) * p.N + row] = __float2bfloat16_rn(s[t]);
+                for (int t = 0; t < NPAD / 8; ++t) {
+                    if (t >= T) continue;
+                    const size_t o = static_cast<size_t>(t) * p.N + row;
+                    if (p.yf)
+                        p.yf[o] = s[t];
+                    else
+                        p.y[o] = __float2bfloat16_rn(s[t]);
+                }
             }
         }
         fence_before_sync();
@@ -725,8 +780,8 @@ __device__ void epilogue(const F4Params& p, int q, int lane, const Work& w, uint
 // --------------------------------------------------------------- kernel
 // Up to 32 MMA columns (t <= 4) two CTAs share an SM (at most 72
 // registers a thread); wider ones run one CTA per SM.
-template <int NPAD>
-__global__ void __launch_bounds__(kThreads, NPAD <= 32 ? 2 : 1)
+template <int NPAD, int IN>
+__global__ void __launch_bounds__(kThreads, NPAD <= 32 && IN == 0 ? 2 : 1)
     f4_linear_kernel(const __grid_constant__ CUtensorMap main_map, const __grid_constant__ CUtensorMap tail_map,
                      const F4Params p) {
     using L = Layout<NPAD>;
@@ -829,7 +884,7 @@ __global__ void __launch_bounds__(kThreads, NPAD <= 32 ? 2 : 1)
             if (lane == 0)
                 mma_issuer<NPAD>(p, w, a_base, lay.slot_a, base + lay.off_b, tbase, sfa_col, sfb_col, bars, wc);
         } else if (warp >= kFirstConverterWarp) {
-            converter<NPAD>(p, warp - kFirstConverterWarp, warp, lane, w, base + lay.off_b, base + lay.off_img, tbase,
+            converter<NPAD, IN>(p, warp - kFirstConverterWarp, warp, lane, w, base + lay.off_b, base + lay.off_img, tbase,
                             sfb_col, bars, wc);
         } else {
             epilogue<NPAD>(p, warp, lane, w, base + lay.off_inbox, base + lay.off_sc, tbase, sfa_col, bars, wc,
@@ -851,14 +906,14 @@ __global__ void __launch_bounds__(kThreads, NPAD <= 32 ? 2 : 1)
 }
 
 // ----------------------------------------------------------------- host
-template <int NPAD>
+template <int NPAD, int IN>
 static cudaError_t launch_npad(const CUtensorMap& main_map, const CUtensorMap& tail_map, const F4Params& p,
                                const F4Plan& plan, cudaStream_t stream) {
     static int configured[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= 64 || configured[dev] < plan.smem_bytes) {
-        cudaError_t e = cudaFuncSetAttribute(f4_linear_kernel<NPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(f4_linear_kernel<NPAD, IN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              plan.smem_bytes);
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) configured[dev] = plan.smem_bytes;
@@ -880,7 +935,7 @@ static cudaError_t launch_npad(const CUtensorMap& main_map, const CUtensorMap& t
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
     }
-    cudaError_t e = cudaLaunchKernelEx(&cfg, f4_linear_kernel<NPAD>, main_map, tail_map, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, f4_linear_kernel<NPAD, IN>, main_map, tail_map, p);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -929,8 +984,8 @@ static bool plan_fit(int npad, int cl, int t, int64_t rows, int64_t groups, int 
     return true;
 }
 
-bool plan_f4(int t, int64_t k, int64_t n, int num_sms, int max_smem, F4Plan* out) {
-    if (t < 1 || t > 8 || k % kStageK != 0 || n < 1 || num_sms < 2) return false;
+bool plan_f4(int t, int64_t k, int64_t n, int num_sms, int max_smem, F4Plan* out, bool swiglu_in) {
+    if (t < 1 || t > (swiglu_in ? 4 : 8) || k % kStageK != 0 || n < 1 || num_sms < 2) return false;
     if (k >= (int64_t(1) << 30) || n >= (int64_t(1) << 30)) return false;
     const int npad = npad_for(t);
     const int64_t stages = k / kStageK;
@@ -958,7 +1013,7 @@ bool plan_f4(int t, int64_t k, int64_t n, int num_sms, int max_smem, F4Plan* out
     // activation buffers, and 512 columns.
     const int half = (max_smem + 1024) / 2 - 1024;
     const int third = (max_smem + 1024) / 3 + 1024;
-    if (npad <= 32)
+    if (npad <= 32 && !swiglu_in)
         for (int na = kMaxNA; na >= 3; --na)
             for (int nb = 4; nb >= 3; --nb)
                 if (plan_fit(npad, cl, t, rows, groups, na, nb, 256, half, third, out)) return true;
@@ -970,11 +1025,16 @@ bool plan_f4(int t, int64_t k, int64_t n, int num_sms, int max_smem, F4Plan* out
 
 cudaError_t launch_f4_linear(const CUtensorMap& main_map, const CUtensorMap& tail_map, const F4Params& p,
                              const F4Plan& plan, cudaStream_t stream) {
+    if (p.xab) {  // t <= 4 (plan_f4)
+        if (plan.npad > 32) return cudaErrorInvalidValue;
+        return plan.npad == 16 ? launch_npad<16, 1>(main_map, tail_map, p, plan, stream)
+                               : launch_npad<32, 1>(main_map, tail_map, p, plan, stream);
+    }
     switch (plan.npad) {
-        case 16: return launch_npad<16>(main_map, tail_map, p, plan, stream);
-        case 32: return launch_npad<32>(main_map, tail_map, p, plan, stream);
-        case 48: return launch_npad<48>(main_map, tail_map, p, plan, stream);
-        default: return launch_npad<64>(main_map, tail_map, p, plan, stream);
+        case 16: return launch_npad<16, 0>(main_map, tail_map, p, plan, stream);
+        case 32: return launch_npad<32, 0>(main_map, tail_map, p, plan, stream);
+        case 48: return launch_npad<48, 0>(main_map, tail_map, p, plan, stream);
+        default: return launch_npad<64, 0>(main_map, tail_map, p, plan, stream);
     }
 }
 

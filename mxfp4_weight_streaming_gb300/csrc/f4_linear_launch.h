@@ -12,9 +12,11 @@ namespace mxfp4 {
 namespace f4 {
 
 struct F4Params {
-    const __nv_bfloat16* x;  // [T, K]
+    const __nv_bfloat16* x;  // [T, K] (unused when xab is set)
+    const float* xab;        // when set: activations SiLU(xab[t, k]) * xab[t, K + k], rows of 2K floats
     const uint8_t* ws;       // [N, K/32] E8M0
-    __nv_bfloat16* y;        // [T, N]
+    __nv_bfloat16* y;        // [T, N] (unused when yf is set)
+    float* yf;               // when set: fp32 outputs [T, N] instead of y
     unsigned* status;        // device status word (bounded-wait timeouts)
     int T, K, N;
     int nblk;       // K / 32
@@ -48,8 +50,10 @@ struct F4Plan {
 };
 
 // False when the shape is outside the kernel's limits (t > 8, k % 512 != 0,
-// or no shared-memory fit).
-bool plan_f4(int t, int64_t k, int64_t n, int num_sms, int max_smem, F4Plan* out);
+// or no shared-memory fit). swiglu_in: the plan of a call with xab set, for
+// t <= 4 only (its conversion holds four loads per unit, two stages ahead:
+// one CTA per SM, and more tokens would spill).
+bool plan_f4(int t, int64_t k, int64_t n, int num_sms, int max_smem, F4Plan* out, bool swiglu_in = false);
 
 // main_map / tail_map: the packed codes as the 3D view (128 B, rows, k/256)
 // with boxes of (128 B, h_main, 2) and (128 B, h_tail, 2) (tail_map unused

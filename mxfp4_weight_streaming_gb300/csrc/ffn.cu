@@ -226,7 +226,9 @@ size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 }  // namespace
 
-size_t ffn_workspace_bytes(int64_t t, int64_t inter) { return 256 + align256(static_cast<size_t>(t * inter) * 4); }
+// A counter word (then h, fp32 [t, inter]) for the cooperative kernel, or
+// a | b (fp32 [t, 2 inter]) for the two-launch chain: both from byte 256.
+size_t ffn_workspace_bytes(int64_t t, int64_t inter) { return 256 + align256(static_cast<size_t>(t * inter) * 8); }
 
 int plan_ffn(int t, int hidden, int inter, int max_smem, FfnPlan* out) {
     FfnPlan pl{};

@@ -998,7 +998,10 @@ bool plan_f4(int t, int64_t k, int64_t n, int num_sms, int max_smem, F4Plan* out
     };
     int cl = 1;
     int64_t rows = rows_for(num_sms);
-    if (rows < 96 && stages >= 2) {
+    // A cluster of 2 also when t > 4 (the conversion's cost per stage
+    // doubles from t = 4 to t = 8): each rank converts half of x, and the
+    // converted stage feeds twice the rows.
+    if ((rows < 96 || npad > 32) && stages >= 2) {
         cl = 2;
         rows = rows_for(num_sms / 2);
     }

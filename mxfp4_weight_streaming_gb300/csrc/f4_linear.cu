@@ -1012,17 +1012,22 @@ bool plan_f4(int t, int64_t k, int64_t n, int num_sms, int max_smem, F4Plan* out
     // prefetches its first weight stages while this call's CTA finishes. The
     // most weight slots (at least 3) next to 3 or 4 activation buffers
     // (kGroups stages are converted at once, and the MMA trails them). Else
-    // one CTA per SM with as many weight slots as fit next to 4 or more
-    // activation buffers, and 512 columns.
+    // one CTA per SM and 512 columns: up to 32 MMA columns, as many weight
+    // slots as fit next to 6 (else 4) activation buffers; wider, the weight
+    // ring first (its refills bound t = 8), next to 3 to 6 buffers.
     const int half = (max_smem + 1024) / 2 - 1024;
     const int third = (max_smem + 1024) / 3 + 1024;
     if (npad <= 32 && !swiglu_in)
         for (int na = kMaxNA; na >= 3; --na)
             for (int nb = 4; nb >= 3; --nb)
                 if (plan_fit(npad, cl, t, rows, groups, na, nb, 256, half, third, out)) return true;
-    for (int nb = 6; nb >= 4; nb -= 2)
-        for (int na = kMaxNA; na >= 2; --na)
-            if (plan_fit(npad, cl, t, rows, groups, na, nb, 512, max_smem, 0, out)) return true;
+    if (npad <= 32)
+        for (int nb = 6; nb >= 4; nb -= 2)
+            for (int na = kMaxNA; na >= 2; --na)
+                if (plan_fit(npad, cl, t, rows, groups, na, nb, 512, max_smem, 0, out)) return true;
+    for (int na = kMaxNA; na >= 2; --na)
+        for (int nb = 6; nb >= 3; --nb)
+            if (nb != 5 && plan_fit(npad, cl, t, rows, groups, na, nb, 512, max_smem, 0, out)) return true;
     return false;
 }
 

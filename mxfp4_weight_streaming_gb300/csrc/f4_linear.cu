@@ -996,16 +996,6 @@ bool plan_f4(int t, int64_t k, int64_t n, int num_sms, int max_smem, F4Plan* out
         const int64_t r = (n + groups - 1) / groups;
         return (r + 7) / 8 * 8;
     };
-    int cl = 1;
-    int64_t rows = rows_for(num_sms);
-    // A cluster of 2 also when t > 4 (the conversion's cost per stage
-    // doubles from t = 4 to t = 8): each rank converts half of x, and the
-    // converted stage feeds twice the rows.
-    if ((rows < 96 || npad > 32) && stages >= 2) {
-        cl = 2;
-        rows = rows_for(num_sms / 2);
-    }
-    const int64_t groups = (n + rows - 1) / rows;
     // Up to 32 MMA columns, prefer plans two CTAs can share an SM with (at
     // most half its shared memory, 256 TMEM columns; launched with more than
     // a third of it, so never three): the next call's CTA then sets up and
@@ -1017,18 +1007,29 @@ bool plan_f4(int t, int64_t k, int64_t n, int num_sms, int max_smem, F4Plan* out
     // ring first (its refills bound t = 8), next to 3 to 6 buffers.
     const int half = (max_smem + 1024) / 2 - 1024;
     const int third = (max_smem + 1024) / 3 + 1024;
-    if (npad <= 32 && !swiglu_in)
-        for (int na = kMaxNA; na >= 3; --na)
-            for (int nb = 4; nb >= 3; --nb)
-                if (plan_fit(npad, cl, t, rows, groups, na, nb, 256, half, third, out)) return true;
-    if (npad <= 32)
-        for (int nb = 6; nb >= 4; nb -= 2)
-            for (int na = kMaxNA; na >= 2; --na)
-                if (plan_fit(npad, cl, t, rows, groups, na, nb, 512, max_smem, 0, out)) return true;
-    for (int na = kMaxNA; na >= 2; --na)
-        for (int nb = 6; nb >= 3; --nb)
-            if (nb != 5 && plan_fit(npad, cl, t, rows, groups, na, nb, 512, max_smem, 0, out)) return true;
-    return false;
+    auto fit = [&](int cl, int64_t rows) -> bool {
+        const int64_t groups = (n + rows - 1) / rows;
+        if (npad <= 32 && !swiglu_in)
+            for (int na = kMaxNA; na >= 3; --na)
+                for (int nb = 4; nb >= 3; --nb)
+                    if (plan_fit(npad, cl, t, rows, groups, na, nb, 256, half, third, out)) return true;
+        if (npad <= 32)
+            for (int nb = 6; nb >= 4; nb -= 2)
+                for (int na = kMaxNA; na >= 2; --na)
+                    if (plan_fit(npad, cl, t, rows, groups, na, nb, 512, max_smem, 0, out)) return true;
+        for (int na = kMaxNA; na >= 2; --na)
+            for (int nb = 6; nb >= 3; --nb)
+                if (nb != 5 && plan_fit(npad, cl, t, rows, groups, na, nb, 512, max_smem, 0, out)) return true;
+        return false;
+    };
+    const int64_t lone = rows_for(num_sms), pair = rows_for(num_sms / 2);
+    // A cluster of 2 also when t > 4 (the conversion's cost per stage
+    // doubles from t = 4 to t = 8): each rank converts half of x, and the
+    // converted stage feeds twice the rows. It needs every tile of the group
+    // in one batch (TMEM), else lone CTAs.
+    if (stages >= 2 && (lone < 96 || npad > 32) && fit(2, pair)) return true;
+    if (lone < 96 && stages >= 2) return false;
+    return fit(1, lone);
 }
 
 cudaError_t launch_f4_linear(const CUtensorMap& main_map, const CUtensorMap& tail_map, const F4Params& p,

@@ -29,15 +29,34 @@ def consumer_warps(t):
     (8, 7168, 7168, 2, 150, 96, 1),
     (1, 1024, 1024, 2, 128, 16, 1),       # 64 clusters of 16 rows
     (1, 7168, 18432, 1, 144, 128, 1),     # FFN up: one 128-row tile per CTA
-    (8, 7168, 18432, 1, 144, 128, 1),
+    (4, 7168, 18432, 1, 144, 128, 1),
+    (8, 7168, 18432, 2, 150, 248, 2),     # t > 4: K in halves, two tiles (128 + 120 rows) per CTA
+    (5, 7168, 18432, 2, 150, 248, 2),
     (4, 7168, 129280, 1, 152, 856, 7),    # LM head: 6 tiles of 128 rows and one of 88 per CTA
+    (6, 7168, 129280, 1, 152, 856, 7),    # t > 4, but 14 tiles per cluster would not fit TMEM: lone CTAs
+    (8, 7168, 129280, 1, 152, 856, 7),
     (3, 512, 64, 1, 8, 8, 1),             # one stage: no K split, 8-row groups
+    (6, 512, 64, 1, 8, 8, 1),
 ])
 def test_packed_e2m1_plans(t, k, n, cluster, ctas, rows, tiles):
     p = mx.linear_plan(t, k, n, SMS, SMEM)
     assert p["mode"] == 4, p
     assert (p["cluster"], p["ctas"], p["group_rows"], p["batch_units"]) == (cluster, ctas, rows, tiles), p
     assert p["stage_steps"] == 2 and p["part_steps"] == 0 and p["ring_slots"] >= 2, p
+
+
+@pytest.mark.parametrize("t,two_per_sm", [(1, True), (2, True), (3, True), (4, True), (5, False), (8, False)])
+def test_packed_e2m1_residency(t, two_per_sm):
+    """Verify width (K = N = 7168): up to 32 MMA columns (t <= 4) a plan
+    within half the SM's shared memory (the next call's CTA shares the SM);
+    wider, one CTA per SM with the weight ring first (at least 5 slots)."""
+    p = mx.linear_plan(t, 7168, 7168, SMS, SMEM)
+    assert p["mode"] == 4, p
+    half = (SMEM + 1024) // 2 - 1024
+    if two_per_sm:
+        assert p["smem_bytes"] <= half and p["ring_slots"] >= 3, p
+    else:
+        assert p["smem_bytes"] > half and p["ring_slots"] >= 5, p
 
 
 @pytest.mark.parametrize("t,k,n,cluster,ctas", [
@@ -102,11 +121,17 @@ def test_plan_invariants_over_shapes():
         if p["mode"] == 4:
             # packed-E2M1 kernel: t <= 8, k % 512; groups of a multiple of 8
             # rows covering n, one per CTA or per 2-CTA cluster (K halves,
-            # only when lone CTAs would get < 96 rows and K has >= 2 stages)
+            # when K has >= 2 stages and lone CTAs would get < 96 rows, or
+            # t > 4 and the cluster's tiles fit one TMEM batch)
             assert k % 512 == 0 and t <= 8, where
             rows, cl = p["group_rows"], p["cluster"]
             lone_rows = -(-(-(-n // SMS)) // 8) * 8
-            assert cl == (2 if lone_rows < 96 and k >= 1024 else 1), where
+            if k >= 1024 and lone_rows < 96:
+                assert cl == 2, where
+            elif k < 1024 or t <= 4:
+                assert cl == 1, where
+            else:
+                assert cl in (1, 2), where
             assert rows % 8 == 0 and rows >= 8 and p["ctas"] == cl * -(-n // rows) <= SMS, where
             assert p["ctas"] // cl * rows >= n > (p["ctas"] // cl - 1) * rows, where
             assert p["batch_units"] == (1 if rows <= 128 else rows // 128 + (rows % 128 != 0)), where

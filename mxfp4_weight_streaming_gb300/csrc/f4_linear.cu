@@ -535,8 +535,12 @@ __device__ void converter(const F4Params& p, int cw, int warp, int lane, const W
                 float h[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
+                    // SiLU(a) * b with the hardware exponential and
+                    // reciprocal: a few ulp of fp32, far below the 16 bits
+                    // below the block maximum that the pieces keep. a very
+                    // negative: 1 + e^-a is inf and the quotient 0.
                     const float a = __uint_as_float(av[i]);
-                    h[i] = a / (1.0f + expf(-a)) * __uint_as_float(bv[i]);  // SiLU(a) * b
+                    h[i] = __fdividef(a, 1.0f + __expf(-a)) * __uint_as_float(bv[i]);
                 }
                 convert_unit_f32(h, (m >> 1) + 2 * u, blk, jj, atom, img, 8 * (m & 1) + blk);
             }

@@ -404,6 +404,10 @@ def run_ours(args, wl_name: str, rank: int, world: int, device, with_cpu_baselin
                      "algorithmic_bytes_per_launch": bytes_call},
         "clocks": clocks.summary(wall0 - 1.5, wall1 + 0.1),
     }
+    # Time x median SM clock: SM cycles per call, comparable across runs
+    # whose clocks differ.
+    if res["clocks"].get("sm_mhz"):
+        res["kcycles_per_call"] = round(us_call * res["clocks"]["sm_mhz"] / 1e3, 3)
     if with_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(wl_name)
     return res

@@ -102,7 +102,7 @@ struct Layout {
     static constexpr int kAtomBytesB = NPAD * kAtomRowBytes;
     static constexpr int kSlotB = 2 * kAtomBytesB;  // a multiple of 1024 (NPAD >= 16)
     static constexpr int kImgBytes = NPAD * 16;
-    static_assert(NPAD % 16 == 0 && NPAD >= 16 && NPAD <= 64, "MMA N");
+    static_assert(NPAD % 16 == 0 && NPAD >= 16 && NPAD <= 128, "MMA N");
     static_assert(kSlotB % 1024 == 0, "B buffers stay 1024-aligned for the 128-byte swizzle");
 
     // Runtime part (depends on NA, NB, the cluster inbox and h_main).
@@ -462,10 +462,12 @@ struct StageCursor {
 
 // Piece scale words into one warp's 32 lanes. Each 32-row quarter of the MMA
 // reads the B scales from its own lanes: B row n at lane n % 32, column
-// (scale address + n / 32); so every warp stores word a of B rows l (v0)
-// and l + 32 (v1) at columns 4a and 4a + 1.
-__device__ __forceinline__ void store_b_scale_words(uint32_t taddr, const uint4& v0, const uint4& v1) {
-    const uint32_t c16[16] = {v0.x, v1.x, 0u, 0u, v0.y, v1.y, 0u, 0u, v0.z, v1.z, 0u, 0u, v0.w, v1.w, 0u, 0u};
+// (scale address + n / 32); so every warp stores word a of B rows l + 32i
+// (vi, i < 4) at column 4a + i.
+__device__ __forceinline__ void store_b_scale_words(uint32_t taddr, const uint4& v0, const uint4& v1,
+                                                    const uint4& v2, const uint4& v3) {
+    const uint32_t c16[16] = {v0.x, v1.x, v2.x, v3.x, v0.y, v1.y, v2.y, v3.y,
+                              v0.z, v1.z, v2.z, v3.z, v0.w, v1.w, v2.w, v3.w};
     tc::tmem_store16(taddr, c16);
     tc::tmem_wait_st();
     fence_before_sync();
@@ -550,8 +552,11 @@ __device__ void converter(const F4Params& p, int cw, int warp, int lane, const W
         if (lane == 0) mbar_arrive(bars.img_ready(cur.slot));
         if (!__all_sync(0xffffffffu, mbar_wait(bars.img_ready(cur.slot), cur.phase, wc))) return false;
         const uint4 v0 = lds128(img + lane * 16);
-        const uint4 v1 = lane + 32 < NPAD ? lds128(img + (lane + 32) * 16) : make_uint4(0u, 0u, 0u, 0u);
-        store_b_scale_words(tbase + lanes + sfb_col + cur.slot * 16, v0, v1);
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        const uint4 v1 = lane + 32 < NPAD ? lds128(img + (lane + 32) * 16) : z;
+        const uint4 v2 = lane + 64 < NPAD ? lds128(img + (lane + 64) * 16) : z;
+        const uint4 v3 = lane + 96 < NPAD ? lds128(img + (lane + 96) * 16) : z;
+        store_b_scale_words(tbase + lanes + sfb_col + cur.slot * 16, v0, v1, v2, v3);
         __syncwarp();
         if (lane == 0) mbar_arrive(bars.full_b(cur.slot));
         cur.next(w.st0, w.spt, nb);
@@ -944,14 +949,15 @@ static cudaError_t launch_npad(const CUtensorMap& main_map, const CUtensorMap& t
     return cudaGetLastError();
 }
 
-static int npad_for(int t) { return t <= 2 ? 16 : (t <= 4 ? 32 : (t <= 6 ? 48 : 64)); }
+static int npad_for(int t) { return t <= 2 ? 16 : (t <= 4 ? 32 : (t <= 6 ? 48 : (t <= 8 ? 64 : 128))); }
 
 static int smem_layout_bytes(int npad, int na, int nb, int inbox, int h_main) {
     switch (npad) {
         case 16: return Layout<16>(na, nb, inbox, h_main).total;
         case 32: return Layout<32>(na, nb, inbox, h_main).total;
         case 48: return Layout<48>(na, nb, inbox, h_main).total;
-        default: return Layout<64>(na, nb, inbox, h_main).total;
+        case 64: return Layout<64>(na, nb, inbox, h_main).total;
+        default: return Layout<128>(na, nb, inbox, h_main).total;
     }
 }
 
@@ -965,7 +971,9 @@ static bool plan_fit(int npad, int cl, int t, int64_t rows, int64_t groups, int 
     const int inbox = cl > 1 ? static_cast<int>(rows) * inbox_vectors(npad) * 16 : 0;
     const int sfa_col = (cols - 16 * na - 16 * nb) / 32 * 32;
     const int max_batch = sfa_col / npad;
-    if (max_batch < 1 || (cl > 1 && max_batch < tiles)) return false;
+    // A cluster hands rank 1's sums of every tile over at once, and above 8
+    // tokens (128 MMA columns) x is converted only once per CTA: one batch.
+    if (max_batch < 1 || ((cl > 1 || t > 8) && max_batch < tiles)) return false;
     int bytes = smem_layout_bytes(npad, na, nb, inbox, h_main) + 1024;  // + alignment slack
     if (bytes > cap) return false;
     bytes = bytes > floor_bytes ? bytes : floor_bytes;
@@ -989,7 +997,7 @@ static bool plan_fit(int npad, int cl, int t, int64_t rows, int64_t groups, int 
 }
 
 bool plan_f4(int t, int64_t k, int64_t n, int num_sms, int max_smem, F4Plan* out, bool swiglu_in) {
-    if (t < 1 || t > (swiglu_in ? 4 : 8) || k % kStageK != 0 || n < 1 || num_sms < 2) return false;
+    if (t < 1 || t > (swiglu_in ? 4 : 16) || k % kStageK != 0 || n < 1 || num_sms < 2) return false;
     if (k >= (int64_t(1) << 30) || n >= (int64_t(1) << 30)) return false;
     const int npad = npad_for(t);
     const int64_t stages = k / kStageK;
@@ -1047,7 +1055,8 @@ cudaError_t launch_f4_linear(const CUtensorMap& main_map, const CUtensorMap& tai
         case 16: return launch_npad<16, 0>(main_map, tail_map, p, plan, stream);
         case 32: return launch_npad<32, 0>(main_map, tail_map, p, plan, stream);
         case 48: return launch_npad<48, 0>(main_map, tail_map, p, plan, stream);
-        default: return launch_npad<64, 0>(main_map, tail_map, p, plan, stream);
+        case 64: return launch_npad<64, 0>(main_map, tail_map, p, plan, stream);
+        default: return launch_npad<128, 0>(main_map, tail_map, p, plan, stream);
     }
 }
 

@@ -104,9 +104,10 @@ def test_linear_k_parts(t, k, n):
     row group, K % 256 != 0 (29 one-step parts, the last one block long),
     partial token tiles (12 of 16, 17 of 32) and CTAs with fewer row groups
     than warps. The last two shapes are the same sizes on the tensor-core
-    kernel (2-CTA clusters over 39-40 tiles of 128 rows, ragged last tile)."""
+    kernels (t = 16: packed E2M1, 69 clusters of 72 rows; t = 17: E4M3 split,
+    2-CTA clusters over 39-40 tiles of 128 rows, ragged last tile)."""
     mx = lib()
-    assert mx.linear_plan(t, k, n)["mode"] == (1 if k % 512 else 3)
+    assert mx.linear_plan(t, k, n)["mode"] == (1 if k % 512 else (4 if t <= 16 else 3))
     w, x = linear_case(80 + t, t, k, n)
     wq, ws, rq, rs = _pack_both(w)
     yg = Guarded((t, n), torch.bfloat16)
@@ -171,7 +172,7 @@ def test_linear_largest_k(t, k, n):
     memory, so each CTA walks K in parts (hundreds of them) with a single
     row group; ragged last row group."""
     mx = lib()
-    assert mx.linear_plan(t, k, n)["mode"] == ((4 if t <= 8 else 3) if k % 512 == 0 else 1)
+    assert mx.linear_plan(t, k, n)["mode"] == ((4 if t <= 16 else 3) if k % 512 == 0 else 1)
     w, x = linear_case(110 + t, t, k, n)
     wq, ws, rq, rs = _pack_both(w)
     y = mx.linear(x, wq, ws)

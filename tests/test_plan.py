@@ -1,9 +1,10 @@
 """The launch plans of mxfp4_linear, checked on the host (no GPU): which
-kernel a shape gets (the packed-E2M1 tensor-core kernel when t <= 8 and
-k % 512 == 0, the E4M3-split tensor-core kernel when t >= 9 and k % 512 ==
-0, else the streaming engine with whole K per CTA, K walked in parts or a
-cluster split of K), and the invariants every plan must keep for the
-kernel's indexing to hold."""
+kernel a shape gets (the packed-E2M1 tensor-core kernel when k % 512 == 0
+and t <= 8, or t <= 16 when each CTA's tiles fit one batch; the E4M3-split
+tensor-core kernel for the other k % 512 == 0 shapes; else the streaming
+engine with whole K per CTA, K walked in parts or a cluster split of K),
+and the invariants every plan must keep for the kernel's indexing to
+hold."""
 import math
 
 import pytest
@@ -37,6 +38,9 @@ def consumer_warps(t):
     (8, 7168, 129280, 1, 152, 856, 7),
     (3, 512, 64, 1, 8, 8, 1),             # one stage: no K split, 8-row groups
     (6, 512, 64, 1, 8, 8, 1),
+    (9, 7168, 7168, 2, 150, 96, 1),       # t = 9-16: 128 MMA columns, x converted once per CTA
+    (16, 7168, 18432, 2, 150, 248, 2),
+    (16, 7168, 4900, 2, 138, 72, 1),
 ])
 def test_packed_e2m1_plans(t, k, n, cluster, ctas, rows, tiles):
     p = mx.linear_plan(t, k, n, SMS, SMEM)
@@ -60,12 +64,12 @@ def test_packed_e2m1_residency(t, two_per_sm):
 
 
 @pytest.mark.parametrize("t,k,n,cluster,ctas", [
-    (9, 7168, 7168, 2, 112),        # 56 tiles of 128 rows, K split over 2-CTA clusters
-    (9, 1024, 1024, 2, 16),
-    (16, 7168, 18432, 1, 144),      # FFN up: one tile per CTA
+    (24, 7168, 7168, 2, 112),       # 56 tiles of 128 rows, K split over 2-CTA clusters
+    (20, 1024, 1024, 2, 16),
+    (17, 7168, 18432, 1, 144),      # FFN up: one tile per CTA
     (32, 7168, 18432, 1, 144),
-    (12, 7168, 129280, 1, 152),     # LM-head width: 1010 tiles over every SM
-    (16, 7168, 4900, 2, 78),
+    (12, 7168, 129280, 1, 152),     # LM-head width at t <= 16: the packed-E2M1 kernel would need 7 tiles in one batch
+    (17, 7168, 4900, 2, 78),
 ])
 def test_tensor_core_plans(t, k, n, cluster, ctas):
     p = mx.linear_plan(t, k, n, SMS, SMEM)
@@ -123,7 +127,7 @@ def test_plan_invariants_over_shapes():
             # rows covering n, one per CTA or per 2-CTA cluster (K halves,
             # when K has >= 2 stages and lone CTAs would get < 96 rows, or
             # t > 4 and the cluster's tiles fit one TMEM batch)
-            assert k % 512 == 0 and t <= 8, where
+            assert k % 512 == 0 and t <= 16, where
             rows, cl = p["group_rows"], p["cluster"]
             lone_rows = -(-(-(-n // SMS)) // 8) * 8
             if k >= 1024 and lone_rows < 96:

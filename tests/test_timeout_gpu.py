@@ -37,8 +37,8 @@ def withhold_lib():
     return L
 
 
-@pytest.mark.parametrize("t,k,n,mode,cluster", [(2, 1056, 256, 0, 1), (12, 1024, 10240, 3, 1), (12, 4096, 256, 3, 2),
-                                               (4, 1024, 20480, 4, 1), (4, 4096, 256, 4, 2)])
+@pytest.mark.parametrize("t,k,n,mode,cluster", [(2, 1056, 256, 0, 1), (20, 1024, 10240, 3, 1), (20, 4096, 256, 3, 2),
+                                               (4, 1024, 20480, 4, 1), (4, 4096, 256, 4, 2), (12, 4096, 256, 4, 2)])
 def test_bounded_wait_runs_out_and_context_survives(withhold_lib, t, k, n, mode, cluster):
     mx = lib()
     plan = mx.linear_plan(t, k, n)

@@ -100,7 +100,9 @@ int mxfp4_quantize(const float* w, int64_t n, int64_t k, uint8_t* wq, uint8_t* w
  * Accumulation is fp32 (tensor-core fp32 accumulate); the summation order
  * is the kernel's. Three kernels serve the call (mxfp4_linear_plan says
  * which):
- *   - t <= 8 and k % 512 == 0: the packed-E2M1 tensor-core kernel
+ *   - k % 512 == 0 and t <= 8, or 9 <= t <= 16 where each CTA's tiles of
+ *     128 rows fit one accumulator batch (dense widths; not the LM head):
+ *     the packed-E2M1 tensor-core kernel
  *     (tcgen05.mma kind::mxf4: the weight codes go from HBM to the tensor
  *     cores as stored, two per byte, with their E8M0 scales). Its other
  *     operand is E2M1 too, so each bf16 activation is written as eight
@@ -113,7 +115,7 @@ int mxfp4_quantize(const float* w, int64_t n, int64_t k, uint8_t* wq, uint8_t* w
  *     below 2^-112, at most 2^-128: the lowest piece scale is 2^-127).
  *   - k % 512 != 0, or t >= 9 with wq not 32-byte aligned: the streaming
  *     engine (E2M1 -> f16 in registers, mma.sync, fp32 block scaling).
- *   - otherwise (9 <= t <= 32): the block-scaled tensor-core kernel
+ *   - otherwise (9 <= t <= 32): the E4M3-split tensor-core kernel
  *     (tcgen05.mma kind::mxf8f6f4: the E2M1 codes and E8M0 scales go to
  *     the tensor cores as stored). Its other operand is 8-bit, so each bf16
  *     activation is split into two E4M3 pieces under one power-of-two scale

@@ -341,9 +341,10 @@ int mxfp4_linear(const void* x, int64_t t, int64_t k, const uint8_t* wq, const u
         }
     if (!plan) {
         LinearPlan fresh;
-        // t <= 8: the packed-E2M1 tensor-core kernel when k % 512 == 0. Then
-        // the E4M3-split tensor-core kernel when the shape and the weight
-        // alignment allow it; the streaming engine otherwise.
+        // The packed-E2M1 tensor-core kernel when its plan fits (k % 512 ==
+        // 0; t <= 8, or t <= 16 with one batch per CTA). Then the E4M3-split
+        // tensor-core kernel when the shape and the weight alignment allow
+        // it; the streaming engine otherwise.
         if (mxfp4::f4::plan_f4(static_cast<int>(t), k, n, d->num_sms, d->max_smem, &fresh.fp)) {
             fresh.kind = 2;
             if (int rc = encode_f4_weight_map(&fresh.map, wq, n, k, fresh.fp.h_main)) return rc;

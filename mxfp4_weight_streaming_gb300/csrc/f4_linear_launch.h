@@ -1,6 +1,6 @@
 // Host interface of the packed-E2M1 tensor-core linear kernel (f4_linear.cu):
 // tcgen05.mma kind::mxf4 with the weights as stored and the activations as
-// eight E2M1 digit pieces, for 1 <= t <= 8.
+// eight E2M1 digit pieces, for 1 <= t <= 16.
 #pragma once
 
 #include <cuda.h>
@@ -49,8 +49,8 @@ struct F4Plan {
     int smem_bytes;  // dynamic shared memory per CTA, as launched
 };
 
-// False when the shape is outside the kernel's limits (t > 8, k % 512 != 0,
-// or no shared-memory fit). swiglu_in: the plan of a call with xab set, for
+// False when the shape is outside the kernel's limits (t > 16, k % 512 != 0,
+// no shared-memory fit, or t > 8 with a CTA's tiles not in one batch). swiglu_in: the plan of a call with xab set, for
 // t <= 4 only (its conversion holds four loads per unit, two stages ahead:
 // one CTA per SM, and more tokens would spill).
 bool plan_f4(int t, int64_t k, int64_t n, int num_sms, int max_smem, F4Plan* out, bool swiglu_in = false);

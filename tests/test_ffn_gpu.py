@@ -35,8 +35,13 @@ def _run(x, dev):
 
 
 @pytest.mark.parametrize("t,hidden,inter", [(1, 256, 128), (4, 512, 256), (5, 256, 384), (8, 1024, 512),
-                                            (3, 96, 160), (2, 2048, 1024), (8, 4096, 1536), (6, 7168, 512)])
+                                            (3, 96, 160), (2, 2048, 1024), (8, 4096, 1536), (6, 7168, 512),
+                                            (3, 1024, 1536), (1, 512, 512), (4, 7168, 512), (2, 1536, 7168)])
 def test_ffn_small(t, hidden, inter):
+    """The two-launch packed-E2M1 chain where t <= 4 and hidden, inter are
+    multiples of 512 (t = 3: padding rows of the MMA's N; hidden = 512: one
+    stage for the up projection; inter = 512: one stage for the down one),
+    the cooperative kernel otherwise."""
     seed = 900 + t + hidden + inter
     dev, _ = _weights(seed, hidden, inter)
     x = synth.tokens(seed, t, hidden, device="cuda")

@@ -1021,10 +1021,17 @@ bool plan_f4(int t, int64_t k, int64_t n, int num_sms, int max_smem, F4Plan* out
     const int third = (max_smem + 1024) / 3 + 1024;
     auto fit = [&](int cl, int64_t rows) -> bool {
         const int64_t groups = (n + rows - 1) / rows;
-        if (npad <= 32 && !swiglu_in)
+        if (npad <= 32 && !swiglu_in) {
             for (int na = kMaxNA; na >= 3; --na)
                 for (int nb = 4; nb >= 3; --nb)
                     if (plan_fit(npad, cl, t, rows, groups, na, nb, 256, half, third, out)) return true;
+            // t <= 2 with one 128-row tile per CTA (the FFN widths): 2
+            // activation buffers (their conversion is short) leave room for
+            // 3 weight slots within half the SM.
+            if (npad == 16 && rows <= kTileRows)
+                for (int na = kMaxNA; na >= 3; --na)
+                    if (plan_fit(npad, cl, t, rows, groups, na, 2, 256, half, third, out)) return true;
+        }
         if (npad <= 32)
             for (int nb = 6; nb >= 4; nb -= 2)
                 for (int na = kMaxNA; na >= 2; --na)

@@ -49,6 +49,16 @@ def test_packed_e2m1_plans(t, k, n, cluster, ctas, rows, tiles):
     assert p["stage_steps"] == 2 and p["part_steps"] == 0 and p["ring_slots"] >= 2, p
 
 
+@pytest.mark.parametrize("t", [1, 2, 3, 4])
+def test_packed_e2m1_residency_ffn_width(t):
+    """FFN-up width (N = 18432, one 128-row tile per CTA): at t <= 2 three
+    32 KB weight slots and two activation buffers fit half the SM, so two
+    CTAs share it; at t = 3-4 they do not, and one CTA runs per SM."""
+    p = mx.linear_plan(t, 7168, 18432, SMS, SMEM)
+    half = (SMEM + 1024) // 2 - 1024
+    assert p["mode"] == 4 and (p["smem_bytes"] <= half) == (t <= 2), p
+
+
 @pytest.mark.parametrize("t,two_per_sm", [(1, True), (2, True), (3, True), (4, True), (5, False), (8, False)])
 def test_packed_e2m1_residency(t, two_per_sm):
     """Verify width (K = N = 7168): up to 32 MMA columns (t <= 4) a plan

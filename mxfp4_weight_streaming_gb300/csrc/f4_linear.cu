@@ -67,7 +67,6 @@ using tc::operand_desc;
 constexpr int kTileRows = 128;      // MMA M
 constexpr int kStageK = 512;        // K values per stage (two atoms)
 constexpr int kAtomRowBytes = 128;  // one atom of one row: 256 packed codes
-constexpr int kPieces = 8;
 constexpr int kEpilogueWarps = 4;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
